@@ -1,0 +1,208 @@
+"""Seeded synthetic inputs for the verify / select / sparse-draft path.
+
+This module only draws random numbers and lays them out (dense logical
+layout for checking, paged layout for the kernels).  It holds none of the
+attention or selection arithmetic, so both the float64 oracle and the CUDA
+path can be fed from it without sharing any of the method's code.
+
+Shapes follow the workloads the method is evaluated on: GQA decoder layers
+shaped like Llama-3-8B (32 query / 8 KV heads, head_dim 128) and Qwen-14B
+(40 / 8, head_dim 128), contexts of 2K to 128K tokens, k = 4..7 drafts, and a
+selection budget of top-k plus sink and recent windows (Vegas: Self-Speculative
+Decoding with Verification-Guided Sparse Attention, "Core claim" and the
+Appendix B sparse-ratio discussion; A Sparse Glimpse of the Whole, "What
+carries the argument").  No dataset is read: the long-context benchmarks the
+pages measure on are stood in for by these seeded tensors.
+
+Heavy hitters: a few prefix keys are pushed toward the mean direction of the
+group's verify queries so that a correct top-k must recover them.  This is an
+input construction, not part of the method.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+from typing import List, Optional
+
+import torch
+
+PAGE_SIZE = 16
+
+
+@dataclass(frozen=True)
+class WorkloadSpec:
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    prefix_lens: tuple            # committed prefix length L_b per sequence
+    n_drafts: int                 # k; the verify block has k+1 rows
+    top_k: int
+    n_sink: int
+    n_recent: int
+    seed: int
+    heavy_frac: float = 0.0       # fraction of candidate positions boosted
+    n_planted: int = 0            # exact count (overrides heavy_frac when > 0)
+    planted_mode: str = "add"     # "add": K += s*sqrt(d)*u ; "replace": K = s*sqrt(d)*u
+    planted_scale: float = 3.0
+    shuffle_pages: bool = False
+    extra_pages: int = 0          # spare physical pages (never referenced)
+    per_head: bool = False
+
+    @property
+    def n_rows(self) -> int:
+        return self.n_drafts + 1
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def max_prefix(self) -> int:
+        return max(self.prefix_lens)
+
+    @property
+    def n_sel_max(self) -> int:
+        return self.n_sink + self.n_recent + self.top_k
+
+
+def _drawn_lengths(n: int, lo: int, hi: int, seed: int) -> tuple:
+    g = torch.Generator().manual_seed(seed)
+    return tuple(int(x) for x in torch.randint(lo, hi + 1, (n,), generator=g))
+
+
+# Named workloads.  Sizes are those of the evaluation the method targets.
+WORKLOADS = {
+    # Single layer, batch 1: 8 q heads / 2 kv heads, head_dim 64, 2K context,
+    # 16 planted keys equal to 4x the query direction; k=4; 128 + 4 + 32.
+    "tiny_d64_2k": WorkloadSpec(
+        name="tiny_d64_2k", batch=1, num_q_heads=8, num_kv_heads=2, head_dim=64,
+        prefix_lens=(2048,), n_drafts=4, top_k=128, n_sink=4, n_recent=32, seed=1,
+        n_planted=16, planted_mode="replace", planted_scale=4.0),
+    # Llama-3-8B-shaped layer, batch 1, 32K context, 1% heavy hitters; k=5;
+    # 2048 + 4 + 64.
+    "llama8b_32k": WorkloadSpec(
+        name="llama8b_32k", batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        prefix_lens=(32768,), n_drafts=5, top_k=2048, n_sink=4, n_recent=64, seed=2,
+        heavy_frac=0.01),
+    # Same layer, batch 8, per-sequence context uniform in [16K, 64K], randomly
+    # permuted page table; both selection modes are exercised.
+    "llama8b_b8_16k_64k": WorkloadSpec(
+        name="llama8b_b8_16k_64k", batch=8, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        prefix_lens=_drawn_lengths(8, 16384, 65536, 3), n_drafts=5, top_k=2048,
+        n_sink=4, n_recent=64, seed=3, heavy_frac=0.01, shuffle_pages=True),
+    # Qwen-14B-shaped layer, batch 1, 128K context, 0.5% heavy hitters; k=7;
+    # 4096 + 4 + 128.
+    "qwen14b_128k": WorkloadSpec(
+        name="qwen14b_128k", batch=1, num_q_heads=40, num_kv_heads=8, head_dim=128,
+        prefix_lens=(131072,), n_drafts=7, top_k=4096, n_sink=4, n_recent=128, seed=4,
+        heavy_frac=0.005),
+}
+
+
+def small_spec(**kw) -> WorkloadSpec:
+    """A small workload for quick parity cases (several tiles, ragged tail)."""
+    base = WorkloadSpec(name="small", batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                        prefix_lens=(1000, 517), n_drafts=3, top_k=64, n_sink=4,
+                        n_recent=16, seed=11, heavy_frac=0.01)
+    return replace(base, **kw)
+
+
+@dataclass
+class Inputs:
+    spec: WorkloadSpec
+    q_verify: torch.Tensor              # bf16 [B][R][Hq][d]
+    k_dense: List[torch.Tensor]         # per b: bf16 [Hkv][n_b][d], n_b = L_b + R
+    v_dense: List[torch.Tensor]
+    draft_q: torch.Tensor               # bf16 [k][B][Hq][d]
+    planted: List[torch.Tensor]         # per b: int64 planted positions
+    page_table: torch.Tensor            # int32 [B][max_pages], -1 = unused
+    k_pages: torch.Tensor               # bf16 [P][Hkv][16][d]
+    v_pages: torch.Tensor
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def prefix_lens(self) -> torch.Tensor:
+        return torch.tensor(self.spec.prefix_lens, dtype=torch.int32)
+
+
+def _unit(x: torch.Tensor) -> torch.Tensor:
+    return x / x.norm()
+
+
+def make_inputs(spec: WorkloadSpec, cache_extra: int = 0) -> Inputs:
+    """Draw all inputs of `spec` on the CPU from its seed.
+
+    cache_extra: additional cache positions per sequence beyond L_b + R
+    (zero-filled K/V, used by tests that append tokens)."""
+    s = spec
+    B, R, Hq, Hkv, d, g = s.batch, s.n_rows, s.num_q_heads, s.num_kv_heads, s.head_dim, s.group
+    assert Hq % Hkv == 0 and len(s.prefix_lens) == B
+    gen = torch.Generator().manual_seed(s.seed)
+    q_verify = torch.randn(B, R, Hq, d, generator=gen).to(torch.bfloat16)
+    k_dense, v_dense, planted = [], [], []
+    for b in range(B):
+        L = s.prefix_lens[b]
+        n = L + R
+        k = torch.randn(Hkv, n + cache_extra, d, generator=gen)
+        v = torch.randn(Hkv, n + cache_extra, d, generator=gen)
+        if cache_extra:
+            k[:, n:] = 0
+            v[:, n:] = 0
+        lo, hi = s.n_sink, max(s.n_sink, L - s.n_recent)
+        n_cand = hi - lo
+        n_pl = s.n_planted if s.n_planted > 0 else int(round(s.heavy_frac * L))
+        n_pl = min(n_pl, n_cand)
+        pos = (torch.randperm(n_cand, generator=gen)[:n_pl] + lo).sort().values
+        if n_pl:
+            qd = q_verify[b].double()                       # [R][Hq][d]
+            for h in range(Hkv):
+                u = _unit(qd[:, h * g:(h + 1) * g, :].sum(dim=(0, 1))).float()
+                amp = s.planted_scale * math.sqrt(d)
+                if s.planted_mode == "replace":
+                    k[h, pos] = amp * u
+                else:
+                    k[h, pos] += amp * u
+        k_dense.append(k.to(torch.bfloat16))
+        v_dense.append(v.to(torch.bfloat16))
+        planted.append(pos)
+    draft_q = torch.randn(s.n_drafts, B, Hq, d, generator=gen).to(torch.bfloat16)
+    page_table, k_pages, v_pages = to_paged(k_dense, v_dense, shuffle=s.shuffle_pages,
+                                            seed=s.seed + 1000, extra_pages=s.extra_pages)
+    return Inputs(spec=s, q_verify=q_verify, k_dense=k_dense, v_dense=v_dense, draft_q=draft_q,
+                  planted=planted, page_table=page_table, k_pages=k_pages, v_pages=v_pages)
+
+
+def to_paged(k_dense, v_dense, shuffle=False, seed=0, extra_pages=0, max_pages=None):
+    """Lay dense per-sequence K/V ([Hkv][n_b][d]) into a page pool
+    [P][Hkv][16][d] plus a page table [B][max_pages] (logical -> physical,
+    -1 where unused).  Positions past n_b inside the last page are zero."""
+    B = len(k_dense)
+    Hkv, _, d = k_dense[0].shape
+    npages = [(k.shape[1] + PAGE_SIZE - 1) // PAGE_SIZE for k in k_dense]
+    total = sum(npages) + extra_pages
+    mp = max(npages) if max_pages is None else max_pages
+    if shuffle:
+        phys = torch.randperm(total, generator=torch.Generator().manual_seed(seed))
+    else:
+        phys = torch.arange(total)
+    kp = torch.zeros(total, Hkv, PAGE_SIZE, d, dtype=k_dense[0].dtype)
+    vp = torch.zeros_like(kp)
+    table = torch.full((B, mp), -1, dtype=torch.int32)
+    off = 0
+    for b in range(B):
+        n = k_dense[b].shape[1]
+        np_b = npages[b]
+        ids = phys[off:off + np_b]
+        off += np_b
+        table[b, :np_b] = ids.to(torch.int32)
+        for src, dst in ((k_dense[b], kp), (v_dense[b], vp)):
+            pad = torch.zeros(Hkv, np_b * PAGE_SIZE, d, dtype=src.dtype)
+            pad[:, :n] = src
+            dst[ids] = pad.view(Hkv, np_b, PAGE_SIZE, d).permute(1, 0, 2, 3)
+    return table, kp, vp
