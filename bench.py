@@ -1,0 +1,381 @@
+"""Decode-step benchmark of the verify -> select -> sparse-draft hot path.
+
+One step = 1 verification attention (k+1 rows, Collect-2 capture) + 1 KV
+selection + k sparse draft attentions, on one seeded synthetic GQA layer.
+
+Timing: CUDA events on the launching stream around each kernel; the L2 is
+flushed (a write larger than L2) before the verify call and before every draft
+call, as other layers would evict it in a real model; the flushes are outside
+the timed segments.  value = mean over K steps of the summed segments.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the path
+shards by sequence with no exchange); the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "llama8b_32k"
+METRIC = "us_per_decode_step"
+METRIC_DESC = "µs per decode step (verify+select+sparse draft) and HBM GB/s vs peak"
+
+
+def algorithmic_bytes(spec, capture_mode=1):
+    """Bytes the method must move per step (bf16 = 2 B): every K and V row read
+    once in verify, the capture written once and read once by select, the
+    selected rows plus tail gathered by every draft step, and Q/O/indices."""
+    B, R, Hq, Hkv, d, k = (spec.batch, spec.n_rows, spec.num_q_heads, spec.num_kv_heads,
+                           spec.head_dim, spec.n_drafts)
+    kv_row = Hkv * d * 2 * 2
+    verify_kv = sum((L + R) * kv_row for L in spec.prefix_lens)
+    qo = 2 * B * R * Hq * d * 2
+    if capture_mode == 1:
+        cap = sum(B_L * Hkv * 4 for B_L in spec.prefix_lens)
+    else:
+        cap = sum(L * Hq * 2 * 4 for L in spec.prefix_lens)
+    n_sel = [min(L, spec.n_sel_max) for L in spec.prefix_lens]
+    idx = sum(n_sel) * 4
+    draft = sum(sum((n + t) * kv_row for n in n_sel) for t in range(1, k + 1))
+    draft_qo = k * 2 * B * Hq * d * 2
+    verify = verify_kv + qo + cap
+    select = cap + idx
+    drafts = draft + draft_qo + k * idx
+    return {"verify": verify, "select": select, "drafts": drafts,
+            "step": verify + select + drafts, "verify_kv": verify_kv}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def verify_traffic(workload):
+    """Per-launch DRAM bytes of the verify kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    src = os.path.join(ROOT, "self_speculative_sparse_vg_gb300", "csrc", "verify.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"verify_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("verify.cu sha256[:16]") != digest:
+        return None
+    try:
+        return int(fields["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", str(gpu_index)], stdout=self.file,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def cpu_baseline(workload, reps=1):
+    """Time the float64 oracle (as it stands) on one full decode step of the
+    workload, single-threaded, in a fresh process."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = f"""
+import sys, time, json
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+from oracle import vg_oracle as O
+from self_speculative_sparse_vg_gb300.workloads import WORKLOADS, make_inputs
+s = WORKLOADS[{workload!r}]
+inp = make_inputs(s)
+q = inp.q_verify.double().numpy()
+k = [x.double().numpy() for x in inp.k_dense]
+v = [x.double().numpy() for x in inp.v_dense]
+dq = inp.draft_q.double().numpy()
+times = []
+for _ in range({reps}):
+    t0 = time.perf_counter()
+    out, rows = O.verify_attention(q, k, v, s.prefix_lens, s.softmax_scale)
+    sel = O.select_kv(O.group_sum(rows, s.num_kv_heads), O.CAPTURE_GROUP_SUM, s.prefix_lens,
+                      s.num_q_heads, s.num_kv_heads, s.top_k, s.n_sink, s.n_recent, s.per_head)
+    for t in range(1, s.n_drafts + 1):
+        O.sparse_draft_attention(dq[t - 1], k, v, sel, s.per_head, s.prefix_lens,
+                                 [L + t for L in s.prefix_lens], s.softmax_scale)
+    times.append(time.perf_counter() - t0)
+print(json.dumps({{"step_s": min(times), "reps": len(times)}}))
+"""
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": res["step_s"] * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
+            "sample": f"one full decode step of {workload} (verify all heads and rows, float64 "
+                      f"selection, {reps} rep(s), best), single thread, float64 numpy"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from self_speculative_sparse_vg_gb300.workloads import WORKLOADS
+    spec = WORKLOADS[args.workload]
+    steps = []
+    for _ in range(args.warmup + args.steps):
+        steps.append(cpu_baseline(args.workload)["value"])
+    timed = steps[args.warmup:]
+    val = statistics.mean(timed)
+    cb = {"value": val, "unit": "us", "cores": 1, "kind": "oracle",
+          "sample": f"each step one full decode step of {args.workload}, single thread"}
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": val, "unit": "us",
+                      "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": val / 1e3, "higher_is_better": False, "scaling": "weak",
+                      "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": _config(spec, args.gpus), "cpu_baseline": cb,
+                      "e2e": {"value": val, "unit": "us", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}))
+
+
+def _config(spec, n):
+    return {"workload": spec.name, "batch": spec.batch, "num_q_heads": spec.num_q_heads,
+            "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+            "prefix_lens": list(spec.prefix_lens) if spec.batch <= 8 else "many",
+            "n_drafts": spec.n_drafts, "top_k": spec.top_k, "n_sink": spec.n_sink,
+            "n_recent": spec.n_recent, "selection": "per_head" if spec.per_head else "head_avg",
+            "capture": "group_sum", "kv": "paged bf16, page 16",
+            "l2": "flushed (write 1.5x L2) before verify and before every draft step",
+            "replicas": n}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from self_speculative_sparse_vg_gb300 import vg
+    from self_speculative_sparse_vg_gb300.step import DecodeStep
+    from self_speculative_sparse_vg_gb300.workloads import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    spec = WORKLOADS[args.workload]
+    inp = make_inputs(spec)
+    st = DecodeStep.create(inp, dev)
+    k = spec.n_drafts
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(int(1.5 * l2), dtype=torch.uint8, device=dev)
+
+    def flush(i):
+        flush_buf.fill_(i & 0xFF)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # ---------------- device-resident timing
+    for i in range(args.warmup):
+        flush(i)
+        st.run()
+    barrier()
+    sampler = ClockSampler(local) if rank == 0 else None
+    marks = []
+    for i in range(args.steps):
+        flush(i)
+        e = [ev() for _ in range(3 + 2 * k)]
+        e[0].record(stream)
+        st.verify()
+        e[1].record(stream)
+        st.select()
+        e[2].record(stream)
+        for t in range(1, k + 1):
+            flush(i + t)
+            e[1 + 2 * t].record(stream)
+            st.draft(t)
+            e[2 + 2 * t].record(stream)
+        marks.append(e)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    assert int(st.error_flag.item()) == 0, "device error flag set"
+    ver = [m[0].elapsed_time(m[1]) * 1e3 for m in marks]
+    sel = [m[1].elapsed_time(m[2]) * 1e3 for m in marks]
+    dra = [sum(m[1 + 2 * t].elapsed_time(m[2 + 2 * t]) * 1e3 for t in range(1, k + 1))
+           for m in marks]
+    step_us = [a + b + c for a, b, c in zip(ver, sel, dra)]
+    local_val = statistics.mean(step_us)
+
+    # ---------------- hot: the step back to back, no flushes
+    barrier()
+    h0, h1 = ev(), ev()
+    h0.record(stream)
+    n_hot = min(args.steps, 500)
+    for _ in range(n_hot):
+        st.run()
+    h1.record(stream)
+    barrier()
+    hot_us = h0.elapsed_time(h1) * 1e3 / n_hot
+
+    # ---------------- end to end through the C ABI with host buffers
+    qv_h = inp.q_verify.pin_memory()
+    dq_h = inp.draft_q.pin_memory()
+    ov_h = torch.empty(st.out_verify.shape, dtype=st.out_verify.dtype).pin_memory()
+    ix_h = torch.empty(st.indices.shape, dtype=st.indices.dtype).pin_memory()
+    ct_h = torch.empty(st.counts.shape, dtype=st.counts.dtype).pin_memory()
+    od_h = torch.empty(st.out_draft.shape, dtype=st.out_draft.dtype).pin_memory()
+    h2d = qv_h.numel() * 2 + dq_h.numel() * 2
+    d2h = ov_h.numel() * 2 + ix_h.numel() * 4 + ct_h.numel() * 4 + od_h.numel() * 2
+    e2e_marks = []
+    n_e2e = min(args.steps, 500)
+    for i in range(n_e2e + args.warmup):
+        flush(i)
+        e = [ev() for _ in range(2 + 2 * k)]
+        e[0].record(stream)
+        st.q_verify.copy_(qv_h, non_blocking=True)
+        st.verify()
+        st.select()
+        ov_h.copy_(st.out_verify, non_blocking=True)
+        ix_h.copy_(st.indices, non_blocking=True)
+        ct_h.copy_(st.counts, non_blocking=True)
+        e[1].record(stream)
+        for t in range(1, k + 1):
+            flush(i + t)
+            e[2 * t].record(stream)
+            st.draft_q[t - 1].copy_(dq_h[t - 1], non_blocking=True)
+            st.draft(t)
+            od_h[t - 1].copy_(st.out_draft[t - 1], non_blocking=True)
+            e[2 * t + 1].record(stream)
+        if i >= args.warmup:
+            e2e_marks.append(e)
+    barrier()
+    e2e_us = statistics.mean(
+        sum(m[2 * j].elapsed_time(m[2 * j + 1]) for j in range(k + 1)) * 1e3 for m in e2e_marks)
+    assert torch.equal(ix_h, st.indices.cpu())
+
+    vals = torch.tensor([local_val, e2e_us, hot_us], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    value, e2e_val, hot_val = (float(x) for x in vals.cpu())
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    nb = algorithmic_bytes(spec)
+    peak, peak_kind = measured_peaks()
+    v_mean = statistics.mean(ver)
+    achieved = nb["verify"] / (v_mean * 1e-6) / 1e9
+    res = {
+        "metric": METRIC, "metric_desc": METRIC_DESC, "value": value, "unit": "us",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see workloads.py)",
+        "config": _config(spec, world),
+        "hbm_gbs_step": nb["step"] / (value * 1e-6) / 1e9,
+        "hbm_frac_step": nb["step"] / (value * 1e-6) / 1e9 / peak,
+        "stages_us": {"verify": v_mean, "select": statistics.mean(sel),
+                      "drafts_total": statistics.mean(dra),
+                      "draft_each": statistics.mean(dra) / max(k, 1)},
+        "stages_bytes": nb,
+        "hot_us_per_step": hot_val,
+        "roofline": {"kernel": "verify_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": verify_traffic(spec.name)},
+        "e2e": {"value": e2e_val, "unit": "us", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * st.launches_per_step(),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        try:
+            res["cpu_baseline"] = cpu_baseline(spec.name)
+        except Exception as exc:  # reported, never fatal
+            res["cpu_baseline"] = {"error": str(exc)[-300:]}
+    print(json.dumps(res))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * vg.h -- C ABI of the verification-guided self-speculative sparse attention
+ * hot path on GB300 (sm_103a).
+ *
+ * Three calls make one decode step of a layer:
+ *   vg_verify_attention        full-KV GQA attention of the k+1 verify rows,
+ *                              capturing two logit rows (Collect-2-Query);
+ *   vg_select_kv               sink + recent + top-k index list from them;
+ *   vg_sparse_draft_attention  decode attention of one draft position over
+ *                              the index list plus the dense tail.
+ *
+ * Sources (page title, section):
+ *   Vegas: Self-Speculative Decoding with Verification-Guided Sparse
+ *   Attention (arXiv 2602.07223) -- "The pith", "Core claim", "What carries
+ *   the argument", Figure 1 and Figure 6 captions, Appendix A.
+ *   A Sparse Glimpse of the Whole: Train-Free Self-Speculative Decoding
+ *   (arXiv 2607.27735) -- "Core claim", "What carries the argument".
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless a comment says otherwise.  The
+ *     caller owns and allocates all memory; the library never allocates,
+ *     frees or synchronises.  Every call is asynchronous on `stream` and
+ *     stream-ordered; per-sequence lengths live on the device and the host
+ *     passes only upper bounds.
+ *   - bf16 means IEEE bfloat16 stored as uint16.
+ *   - Host-detectable problems return a status and launch nothing.
+ *   - Device-detectable problems (page id out of range, index out of range,
+ *     a length above the host bound, a pipeline wait that timed out) OR a
+ *     VG_DEVERR_* bit into *error_flag (when error_flag is not NULL) and skip
+ *     the offending load or sequence; nothing traps.
+ *   - Workspaces: sized by the matching *_workspace_bytes() call for the same
+ *     arguments on the same device.  A workspace must be zero-filled once
+ *     before its first use; every completed call leaves it reusable (its
+ *     counters return to zero).  Calls that share a workspace must not
+ *     overlap in time.
+ */
+#ifndef VG_H_
+#define VG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vg_status {
+  VG_OK = 0,
+  VG_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, inconsistent shape */
+  VG_ERR_UNSUPPORTED = 2,        /* valid but outside the supported shapes        */
+  VG_ERR_WORKSPACE_TOO_SMALL = 3,
+  VG_ERR_LAUNCH = 4              /* a CUDA call failed; see cudaGetLastError()    */
+} vg_status;
+
+/* What vg_verify_attention writes to `capture`. */
+enum {
+  VG_CAPTURE_NONE = 0,
+  /* float32 [batch][num_kv_heads][max_prefix]:
+   *   G[b][h][j] = sum over the query heads q of KV head h, ascending, of
+   *                (s[q][row 0][j] + s[q][row k][j]),
+   *   accumulated in float32 as acc = pair(q0); acc = acc + pair(q1); ...   */
+  VG_CAPTURE_GROUP_SUM = 1,
+  /* float32 [batch][num_q_heads][2][max_prefix]: slot 0 = row 0 (first draft
+   * token), slot 1 = row k (bonus token).  With n_rows == 1 both slots hold
+   * row 0.                                                                  */
+  VG_CAPTURE_ROWS = 2
+};
+
+/* Bits OR-ed into *error_flag by the kernels. */
+enum {
+  VG_DEVERR_PAGE = 1,     /* page-table entry outside [0, num_pages)          */
+  VG_DEVERR_INDEX = 2,    /* selected index outside [0, tail_start)           */
+  VG_DEVERR_COUNT = 4,    /* selected count outside [0, cap]                  */
+  VG_DEVERR_TIMEOUT = 8,  /* a bounded pipeline wait gave up                  */
+  VG_DEVERR_LENGTH = 16   /* a device length exceeds its host-side bound      */
+};
+
+/* Paged KV cache.  Pages hold 16 consecutive positions of one sequence.
+ *   k_pages, v_pages: bf16 [num_pages][num_kv_heads][page_size][head_dim];
+ *                     base 16-byte aligned.  One (page, head) chunk is
+ *                     contiguous (4 KB at head_dim 128).
+ *   page_table:       int32 [batch][max_pages_per_seq]; logical page p of
+ *                     sequence b is physical page page_table[b][p].  Entries
+ *                     past a sequence's last page are never read.
+ * Cache slots of the last page past a sequence's length may hold anything.  */
+typedef struct vg_paged_kv {
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* page_table;
+  int32_t num_pages;
+  int32_t page_size;           /* must be 16                    */
+  int32_t max_pages_per_seq;
+  int32_t num_kv_heads;
+  int32_t head_dim;            /* 64 or 128                     */
+} vg_paged_kv;
+
+/* ---------------------------------------------------------------------------
+ * Verification attention with Collect-2-Query capture.
+ * Vegas, "Core claim" and Figure 6: one full-attention pass over the cache
+ * verifies the k drafts plus the bonus position and writes only the
+ * pre-softmax logit rows of the first draft token and of the bonus token.
+ *
+ *   q            bf16 [batch][n_rows][num_q_heads][head_dim], n_rows = k+1.
+ *   prefix_lens  int32 [batch], 1 <= L_b <= max_prefix.  Verify row i of
+ *                sequence b sits at position L_b + i and attends positions
+ *                [0, L_b + i] (its own K/V must already be in the cache).
+ *   softmax_scale  logits are softmax_scale * q.k (1/sqrt(head_dim) for the
+ *                usual attention; 1 captures the raw qK^T).
+ *   out          bf16 [batch][n_rows][num_q_heads][head_dim].
+ *   capture      see VG_CAPTURE_*; only prefix positions j < L_b are
+ *                written, the rest of each row is left untouched.  May be
+ *                NULL with VG_CAPTURE_NONE.
+ *   num_splits   0 = automatic; otherwise the number of KV-length splits
+ *                (clamped to the number of 64-position tiles).  Results agree
+ *                across split counts up to float32 rounding.
+ * Supported: head_dim 64/128, page_size 16, group g = num_q_heads /
+ * num_kv_heads in [1, 8], g * n_rows <= 96, n_rows <= 16.
+ * ------------------------------------------------------------------------- */
+size_t vg_verify_workspace_bytes(int batch, int n_rows, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int max_prefix, int num_splits);
+
+vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q, const int32_t* prefix_lens,
+                              int batch, int n_rows, int num_q_heads, int max_prefix,
+                              float softmax_scale, void* out, int capture_mode, float* capture,
+                              int num_splits, void* workspace, size_t workspace_bytes,
+                              int32_t* error_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Verification-guided KV selection.
+ * Vegas, "Core claim": combine the two captured rows across the query heads
+ * and keep the top-k prefix positions.  A Sparse Glimpse of the Whole, "What
+ * carries the argument": always keep sink and recent tokens; per-head index
+ * variant.
+ *
+ * For each selection row (one per sequence, or one per KV head when
+ * per_head != 0) the score of prefix position j is
+ *   per_head == 0:  sum over KV heads h ascending of G[b][h][j]  (float32,
+ *                   acc = G[0]; acc = acc + G[1]; ...),
+ *   per_head != 0:  G[b][h][j],
+ * where G is the capture itself (VG_CAPTURE_GROUP_SUM) or is formed from
+ * VG_CAPTURE_ROWS in the order documented above.  The result is
+ *   [0, n_sink) u [L_b - n_recent, L_b) u (the top_k positions of
+ *   [n_sink, L_b - n_recent) by score descending, lower position first on
+ *   equal scores),
+ * or all of [0, L_b) when L_b <= n_sink + n_recent + top_k.  -0.0 ranks as
+ * +0.0.  Scores must not be NaN.
+ *
+ *   indices  int32 [batch][rows][cap], ascending, entries past the count = -1.
+ *   counts   int32 [batch][rows].
+ *   cap      >= min(max_prefix, n_sink + n_recent + top_k).
+ * Supported: max_prefix <= 262144.
+ * ------------------------------------------------------------------------- */
+size_t vg_select_workspace_bytes(int batch, int num_kv_heads, int max_prefix, int per_head);
+
+vg_status vg_select_kv(const float* capture, int capture_mode, const int32_t* prefix_lens,
+                       int batch, int num_q_heads, int num_kv_heads, int max_prefix, int top_k,
+                       int n_sink, int n_recent, int per_head, int32_t* indices, int32_t* counts,
+                       int cap, void* workspace, size_t workspace_bytes, int32_t* error_flag,
+                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Sparse draft attention.
+ * Vegas, "Core claim" and Figure 1: while drafting, each draft token attends
+ * only the selected KV entries; the positions produced since the selection
+ * (the dense tail) are attended in full.
+ *
+ *   q           bf16 [batch][num_q_heads][head_dim], one draft position per
+ *               sequence, at position cur_len[b] - 1.
+ *   indices, counts  as written by vg_select_kv (per_head must match);
+ *               every index must be < tail_start[b].
+ *   tail_start  int32 [batch]: the prefix length the selection was made on.
+ *   cur_len     int32 [batch]: query position + 1; tail = [tail_start,
+ *               cur_len), 0 <= cur_len - tail_start <= max_tail.
+ *   out         bf16 [batch][num_q_heads][head_dim].
+ * The attended list (selection, then tail) is processed in chunks of 64
+ * entries, one CTA each, merged by the last CTA to finish.
+ * Supported: head_dim 64/128, g in [1, 8].
+ * ------------------------------------------------------------------------- */
+size_t vg_sparse_draft_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int cap, int max_tail);
+
+vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void* q, const int32_t* indices,
+                                    const int32_t* counts, int per_head, int cap,
+                                    const int32_t* tail_start, const int32_t* cur_len, int batch,
+                                    int num_q_heads, int max_tail, float softmax_scale, void* out,
+                                    void* workspace, size_t workspace_bytes,
+                                    int32_t* error_flag, cudaStream_t stream);
+
+/* Static string for a status code (host). */
+const char* vg_status_string(vg_status status);
+
+/* Library version, e.g. "0.1.0" (host). */
+const char* vg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VG_H_ */

@@ -82,6 +82,24 @@ def verify_attention(q, k, v, prefix_lens, scale):
     return out, rows
 
 
+def capture_rows(q, k, prefix_lens, scale):
+    """Only the Collect-2-Query rows of verify_attention, for large inputs:
+    rows[b,h,0,j] = scale*q_{b,0,h}.k_j and rows[b,h,1,j] = scale*q_{b,k,h}.k_j
+    for prefix positions j < L_b (NaN beyond).  [Vegas] "Core claim"."""
+    B, R, Hq, d = q.shape
+    Hkv = k[0].shape[0]
+    g = Hq // Hkv
+    Lmax = int(max(prefix_lens))
+    rows = np.full((B, Hq, 2, Lmax), np.nan)
+    for b in range(B):
+        L = int(prefix_lens[b])
+        for h in range(Hq):
+            kp = k[b][h // g, :L]
+            rows[b, h, 0, :L] = scale * (kp @ q[b, 0, h])
+            rows[b, h, 1, :L] = scale * (kp @ q[b, R - 1, h])
+    return rows
+
+
 def group_sum(rows, num_kv_heads):
     """G[b,h,j] = sum over the query heads q of KV head h of
     (row0[q,j] + rowk[q,j]), float64.  [Vegas] "What carries the argument":

@@ -1,0 +1,341 @@
+// Verification-guided KV selection: sink + recent + top-k (sm_103a).
+//
+// Vegas: Self-Speculative Decoding with Verification-Guided Sparse Attention,
+// "Core claim": combine the captured first-draft and bonus logit rows across
+// the query heads and keep the top-k prefix positions.  A Sparse Glimpse of
+// the Whole, "What carries the argument": sink and recent tokens are always
+// kept; per-head index variant.
+//
+// Design: one thread-block cluster of C CTAs per selection row.  CTA c owns a
+// contiguous slice of positions, forms the fp32 scores in the documented
+// order, maps them to order-preserving 32-bit keys held in shared memory, and
+// takes part in a 4-pass MSB-first 8-bit radix select whose 256-bin
+// histograms are summed across the cluster through distributed shared memory
+// (double-buffered, one cluster barrier per pass).  That yields the exact
+// top_k-th key T.  Keys > T are all kept; keys == T are kept by ascending
+// position, using exclusive per-CTA counts exchanged across the cluster; each
+// CTA then writes its kept positions in order straight into their final
+// slots.  The result is deterministic and equals a stable sort by
+// (score desc, position asc).
+#include <cooperative_groups.h>
+
+#include "vg_device.cuh"
+#include "vg_host.h"
+
+namespace cg = cooperative_groups;
+
+namespace vg {
+namespace {
+
+constexpr int kSelThreads = 1024;
+constexpr int kMaxCluster = 16;
+constexpr int kTargetSlice = 4096;
+constexpr int kMaxSlice = 16384;  // keys per CTA (64 KB of shared memory)
+
+struct SelectParams {
+  const float* capture;
+  const int32_t* prefix_lens;
+  int32_t* indices;
+  int32_t* counts;
+  int32_t* error_flag;
+  int capture_mode, batch, num_q_heads, num_kv_heads, group, max_prefix;
+  int top_k, n_sink, n_recent, per_head, cap, rows, slice;
+};
+
+// Order-preserving map float -> uint32 (larger float -> larger key), -0 as +0.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Score of prefix position j for selection row `row` of sequence b, summed in
+// the order documented in vg.h (plain fp32 adds, no reassociation).
+__device__ __forceinline__ float row_score(const SelectParams& p, int b, int row, int j) {
+  const size_t L = p.max_prefix;
+  if (p.capture_mode == VG_CAPTURE_GROUP_SUM) {
+    const float* G = p.capture + (size_t)b * p.num_kv_heads * L + j;
+    if (p.per_head) return __ldg(G + (size_t)row * L);
+    float acc = __ldg(G);
+    for (int h = 1; h < p.num_kv_heads; ++h) acc = acc + __ldg(G + (size_t)h * L);
+    return acc;
+  }
+  const float* Rw = p.capture + (size_t)b * p.num_q_heads * 2 * L + j;  // [q][2][L]
+  const int g = p.group;
+  const int h0 = p.per_head ? row : 0, h1 = p.per_head ? row + 1 : p.num_kv_heads;
+  float acc = 0.f;
+  for (int h = h0; h < h1; ++h) {
+    const int q0 = h * g;
+    float G = __ldg(Rw + (size_t)(2 * q0) * L) + __ldg(Rw + (size_t)(2 * q0 + 1) * L);
+    for (int qi = 1; qi < g; ++qi) {
+      const int q = q0 + qi;
+      G = G + (__ldg(Rw + (size_t)(2 * q) * L) + __ldg(Rw + (size_t)(2 * q + 1) * L));
+    }
+    acc = (h == h0) ? G : acc + G;
+  }
+  return acc;
+}
+
+// Exclusive block-wide count of a per-thread flag; *total = block sum.
+__device__ __forceinline__ int block_excl_count(bool f, int* wb, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const unsigned bal = __ballot_sync(0xffffffffu, f);
+  if (lane == 0) wb[warp] = __popc(bal);
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nw ? wb[lane] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    wb[32 + lane] = incl - v;
+    if (lane == 31) wb[64] = incl;
+  }
+  __syncthreads();
+  const int r = wb[32 + warp] + __popc(bal & ((1u << lane) - 1u));
+  *total = wb[64];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectParams p) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  __shared__ uint32_t hist[2][256];
+  __shared__ uint32_t tot_s[256];
+  __shared__ int cnt[2];    // this CTA's candidate keys > T and == T
+  __shared__ int ctl[4];    // digit, remaining k, gt_before, eq_before
+  __shared__ int wb[96];
+  extern __shared__ __align__(16) uint32_t keys[];  // [slice]
+
+  const int L = p.prefix_lens[b];
+  int32_t* out = p.indices + ((size_t)b * p.rows + row) * p.cap;
+  if (L < 0 || L > p.max_prefix) {  // same decision in every CTA of the cluster
+    if (tid == 0 && rank == 0) flag_error(p.error_flag, VG_DEVERR_LENGTH);
+    return;
+  }
+  const int budget = p.n_sink + p.n_recent + p.top_k;
+  const int lo = rank * p.slice;
+  const int n_loc = max(0, min(lo + p.slice, L) - lo);
+
+  if (L <= budget) {  // every prefix position is kept
+    for (int j = tid; j < n_loc; j += blockDim.x) out[lo + j] = lo + j;
+    if (rank == 0) {
+      for (int j = L + tid; j < p.cap; j += blockDim.x) out[j] = -1;
+      if (tid == 0) p.counts[(size_t)b * p.rows + row] = L;
+    }
+    return;
+  }
+  const int c_lo = p.n_sink, c_hi = L - p.n_recent;  // candidates [c_lo, c_hi)
+
+  for (int j = tid; j < n_loc; j += blockDim.x) keys[j] = score_key(row_score(p, b, row, lo + j));
+  __syncthreads();
+
+  // ---- exact top_k-th largest candidate key: 4 passes of 8 bits, MSB first
+  uint32_t prefix = 0, mask = 0;
+  int krem = p.top_k;
+  const int iters = (n_loc + blockDim.x - 1) / blockDim.x;
+  if (p.top_k > 0) {
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      uint32_t* hb = hist[pass & 1];
+      if (tid < 256) hb[tid] = 0;
+      __syncthreads();
+      for (int it = 0; it < iters; ++it) {
+        const int j = it * blockDim.x + tid;
+        const int pos = lo + j;
+        const bool in = j < n_loc && pos >= c_lo && pos < c_hi;
+        const uint32_t key = in ? keys[j] : 0u;
+        const bool v = in && ((key & mask) == prefix);
+        const int dig = v ? (int)((key >> shift) & 255u) : -1;
+        const unsigned grp = __match_any_sync(0xffffffffu, dig);
+        if (v && lane == __ffs(grp) - 1) atomicAdd(&hb[dig], (uint32_t)__popc(grp));
+      }
+      cluster.sync();
+      if (tid < 256) {
+        uint32_t t = 0;
+        for (int c = 0; c < C; ++c) t += cluster.map_shared_rank(hb, c)[tid];
+        tot_s[tid] = t;
+      }
+      __syncthreads();
+      if (tid < 32) {
+        // lane owns digits [8 lane, 8 lane + 8); suffix sums run from digit 255 down
+        uint32_t own = 0;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) own += tot_s[8 * lane + d];
+        uint32_t incl = own;  // sum over lanes >= lane
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_down_sync(0xffffffffu, incl, o);
+          if (lane + o < 32) incl += t;
+        }
+        uint32_t above = incl - own;  // keys with a digit above this lane's range
+        for (int d = 8 * lane + 7; d >= 8 * lane; --d) {
+          const uint32_t t = tot_s[d];
+          if (above < (uint32_t)krem && above + t >= (uint32_t)krem) {
+            ctl[0] = d;
+            ctl[1] = krem - (int)above;
+          }
+          above += t;
+        }
+      }
+      __syncthreads();
+      prefix |= (uint32_t)ctl[0] << shift;
+      mask |= 255u << shift;
+      krem = ctl[1];
+      __syncthreads();
+    }
+  }
+  const uint32_t T = prefix;  // exact key of the top_k-th candidate; krem of the == T keys are kept
+
+  // ---- per-CTA counts of > T and == T, exclusive prefix over lower ranks
+  if (tid < 2) cnt[tid] = 0;
+  __syncthreads();
+  if (p.top_k > 0) {
+    int gt = 0, eq = 0;
+    for (int j = tid; j < n_loc; j += blockDim.x) {
+      const int pos = lo + j;
+      if (pos >= c_lo && pos < c_hi) {
+        const uint32_t k = keys[j];
+        gt += k > T;
+        eq += k == T;
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o);
+      eq += __shfl_xor_sync(0xffffffffu, eq, o);
+    }
+    if (lane == 0) {
+      atomicAdd(&cnt[0], gt);
+      atomicAdd(&cnt[1], eq);
+    }
+  }
+  cluster.sync();
+  if (tid == 0) {
+    int gb = 0, eb = 0;
+    for (int c = 0; c < rank; ++c) {
+      const int* rc = cluster.map_shared_rank(cnt, c);
+      gb += rc[0];
+      eb += rc[1];
+    }
+    ctl[2] = gb;
+    ctl[3] = eb;
+  }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
+
+  if (p.top_k > 0) {
+    const int gt_before = ctl[2], eq_before = ctl[3];
+    const int take_eq = max(0, min(krem - eq_before, cnt[1]));
+    const int sel_before = gt_before + min(eq_before, krem);
+    int eq_run = 0, sel_run = 0;
+    for (int it = 0; it < iters; ++it) {
+      const int j = it * blockDim.x + tid;
+      const int pos = lo + j;
+      const bool in = j < n_loc && pos >= c_lo && pos < c_hi;
+      const uint32_t k = in ? keys[j] : 0u;
+      const bool is_gt = in && k > T, is_eq = in && k == T;
+      int tot;
+      const int eq_rank = eq_run + block_excl_count(is_eq, wb, &tot);
+      eq_run += tot;
+      const bool sel = is_gt || (is_eq && eq_rank < take_eq);
+      const int slot = p.n_sink + sel_before + sel_run + block_excl_count(sel, wb, &tot);
+      sel_run += tot;
+      if (sel) out[slot] = pos;
+    }
+  }
+  if (rank == 0) {
+    for (int j = tid; j < p.n_sink; j += blockDim.x) out[j] = j;
+    for (int j = tid; j < p.n_recent; j += blockDim.x)
+      out[p.n_sink + p.top_k + j] = L - p.n_recent + j;
+    for (int j = budget + tid; j < p.cap; j += blockDim.x) out[j] = -1;
+    if (tid == 0) p.counts[(size_t)b * p.rows + row] = budget;
+  }
+}
+
+bool select_shape(int max_prefix, int* C, int* slice) {
+  int c = 1;
+  while (c < 8 && ceil_div(max_prefix, c) > kTargetSlice) c *= 2;
+  while (c < kMaxCluster && ceil_div(max_prefix, c) > kMaxSlice) c *= 2;
+  const int s = align_up(ceil_div(max_prefix, c), 4);
+  if (s > kMaxSlice) return false;
+  *C = c;
+  *slice = s;
+  return true;
+}
+
+}  // namespace
+}  // namespace vg
+
+using namespace vg;
+
+extern "C" size_t vg_select_workspace_bytes(int, int, int, int) { return 0; }
+
+extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
+                                  const int32_t* prefix_lens, int batch, int num_q_heads,
+                                  int num_kv_heads, int max_prefix, int top_k, int n_sink,
+                                  int n_recent, int per_head, int32_t* indices, int32_t* counts,
+                                  int cap, void* /*workspace*/, size_t /*workspace_bytes*/,
+                                  int32_t* error_flag, cudaStream_t stream) {
+  if (!capture || !prefix_lens || !indices || !counts || batch <= 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || max_prefix <= 0 || top_k < 0 || n_sink < 0 || n_recent < 0 || cap <= 0)
+    return VG_ERR_INVALID_ARGUMENT;
+  if (capture_mode != VG_CAPTURE_GROUP_SUM && capture_mode != VG_CAPTURE_ROWS)
+    return VG_ERR_INVALID_ARGUMENT;
+  if (num_q_heads % num_kv_heads) return VG_ERR_INVALID_ARGUMENT;
+  const long long budget = (long long)n_sink + n_recent + top_k;
+  if (cap < std::min<long long>(max_prefix, budget)) return VG_ERR_INVALID_ARGUMENT;
+  int C, slice;
+  if (!select_shape(max_prefix, &C, &slice)) return VG_ERR_UNSUPPORTED;
+
+  SelectParams p;
+  p.capture = capture;
+  p.prefix_lens = prefix_lens;
+  p.indices = indices;
+  p.counts = counts;
+  p.error_flag = error_flag;
+  p.capture_mode = capture_mode;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.max_prefix = max_prefix;
+  p.top_k = top_k;
+  p.n_sink = n_sink;
+  p.n_recent = n_recent;
+  p.per_head = per_head ? 1 : 0;
+  p.cap = cap;
+  p.rows = per_head ? num_kv_heads : 1;
+  p.slice = slice;
+
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxSlice * 4) != cudaSuccess ||
+        cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+      return VG_ERR_LAUNCH;
+    attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, p.rows, batch);
+  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)slice * 4;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel, p);
+  return e == cudaSuccess ? VG_OK : VG_ERR_LAUNCH;
+}

@@ -1,0 +1,100 @@
+"""One decode step of one layer through the C ABI: verify (k+1 rows, capture)
+-> select -> k sparse draft calls.  Holds the device buffers of a workload;
+every computation happens in libvg's kernels."""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+from . import vg
+from .workloads import Inputs, WorkloadSpec
+
+
+@dataclass
+class DecodeStep:
+    spec: WorkloadSpec
+    device: torch.device
+    kv: vg.PagedKV
+    q_verify: torch.Tensor          # [B][R][Hq][d]
+    draft_q: torch.Tensor           # [k][B][Hq][d]
+    prefix_lens: torch.Tensor       # int32 [B]
+    capture_mode: int
+    per_head: bool
+    capture: torch.Tensor
+    out_verify: torch.Tensor
+    indices: torch.Tensor
+    counts: torch.Tensor
+    out_draft: torch.Tensor         # [k][B][Hq][d]
+    tail_start: torch.Tensor
+    cur_len: torch.Tensor           # [k][B]
+    ws_verify: torch.Tensor
+    ws_draft: torch.Tensor
+    error_flag: torch.Tensor
+    num_splits: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @classmethod
+    def create(cls, inp: Inputs, device="cuda", capture_mode=vg.CAPTURE_GROUP_SUM,
+               per_head: Optional[bool] = None, num_splits=0):
+        s = inp.spec
+        dev = torch.device(device)
+        per_head = s.per_head if per_head is None else per_head
+        B, R, Hq, Hkv, d = s.batch, s.n_rows, s.num_q_heads, s.num_kv_heads, s.head_dim
+        Lmax = s.max_prefix
+        kv = vg.PagedKV(inp.k_pages.to(dev), inp.v_pages.to(dev), inp.page_table.to(dev))
+        if capture_mode == vg.CAPTURE_ROWS:
+            capture = torch.zeros(B, Hq, 2, Lmax, dtype=torch.float32, device=dev)
+        else:
+            capture = torch.zeros(B, Hkv, Lmax, dtype=torch.float32, device=dev)
+        rows = Hkv if per_head else 1
+        cap = min(Lmax, s.n_sel_max)
+        prefix = torch.tensor(s.prefix_lens, dtype=torch.int32, device=dev)
+        k = s.n_drafts
+        cur = torch.stack([prefix + t for t in range(1, k + 1)]) if k else prefix[None][:0]
+        wsv = vg.zero_workspace(vg.verify_workspace_bytes(B, R, Hq, Hkv, d, Lmax, num_splits), dev)
+        wsd = vg.zero_workspace(vg.sparse_draft_workspace_bytes(B, Hq, Hkv, d, cap, max(k, 1)), dev)
+        return cls(spec=s, device=dev, kv=kv, q_verify=inp.q_verify.to(dev),
+                   draft_q=inp.draft_q.to(dev), prefix_lens=prefix, capture_mode=capture_mode,
+                   per_head=per_head, capture=capture,
+                   out_verify=torch.zeros(B, R, Hq, d, dtype=torch.bfloat16, device=dev),
+                   indices=torch.full((B, rows, cap), -7, dtype=torch.int32, device=dev),
+                   counts=torch.zeros(B, rows, dtype=torch.int32, device=dev),
+                   out_draft=torch.zeros(max(k, 1), B, Hq, d, dtype=torch.bfloat16, device=dev),
+                   tail_start=prefix.clone(), cur_len=cur.contiguous(), ws_verify=wsv,
+                   ws_draft=wsd, error_flag=torch.zeros(1, dtype=torch.int32, device=dev),
+                   num_splits=num_splits)
+
+    @property
+    def max_tail(self):
+        return max(self.spec.n_drafts, 1)
+
+    def verify(self, stream=None):
+        s = self.spec
+        vg.verify_attention(self.kv, self.q_verify, self.prefix_lens, s.max_prefix, s.softmax_scale,
+                            self.out_verify, self.capture_mode, self.capture, self.num_splits,
+                            self.ws_verify, self.error_flag, stream)
+
+    def select(self, stream=None):
+        s = self.spec
+        vg.select_kv(self.capture, self.capture_mode, self.prefix_lens, s.num_q_heads,
+                     s.num_kv_heads, s.max_prefix, s.top_k, s.n_sink, s.n_recent, self.per_head,
+                     self.indices, self.counts, self.error_flag, stream)
+
+    def draft(self, t: int, stream=None):
+        """Draft step t = 1..k: query at position L + t - 1, tail [L, L + t)."""
+        s = self.spec
+        vg.sparse_draft_attention(self.kv, self.draft_q[t - 1], self.indices, self.counts,
+                                  self.per_head, self.tail_start, self.cur_len[t - 1],
+                                  self.max_tail, s.softmax_scale, self.out_draft[t - 1],
+                                  self.ws_draft, self.error_flag, stream)
+
+    def run(self, stream=None):
+        self.verify(stream)
+        self.select(stream)
+        for t in range(1, self.spec.n_drafts + 1):
+            self.draft(t, stream)
+
+    def launches_per_step(self) -> int:
+        return 2 + self.spec.n_drafts

@@ -1,0 +1,190 @@
+"""Thin Python binding of libvg.so (the C ABI in include/vg.h).
+
+Argument marshalling only: tensors in, device pointers and sizes out, the
+current torch stream passed through.  Every step of the hot path runs in the
+library's CUDA kernels; if the library is missing this module raises on
+import -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvg.so")
+
+CAPTURE_NONE = 0
+CAPTURE_GROUP_SUM = 1
+CAPTURE_ROWS = 2
+
+DEVERR_PAGE = 1
+DEVERR_INDEX = 2
+DEVERR_COUNT = 4
+DEVERR_TIMEOUT = 8
+DEVERR_LENGTH = 16
+
+EXPORTED = (
+    "vg_verify_workspace_bytes", "vg_verify_attention",
+    "vg_select_workspace_bytes", "vg_select_kv",
+    "vg_sparse_draft_workspace_bytes", "vg_sparse_draft_attention",
+    "vg_status_string", "vg_version",
+)
+
+
+class VGError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+class PagedKVStruct(ctypes.Structure):
+    _fields_ = [("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("num_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; "
+                          f"g.build()\"` (needs nvcc with sm_103a support)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    kvp = ctypes.POINTER(PagedKVStruct)
+    sig = {
+        "vg_verify_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+        "vg_verify_attention": (i32, [kvp, vp, vp, i32, i32, i32, i32, f32, vp, i32, vp, i32,
+                                      vp, sz, vp, vp]),
+        "vg_select_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "vg_select_kv": (i32, [vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, i32,
+                               vp, sz, vp, vp]),
+        "vg_sparse_draft_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+        "vg_sparse_draft_attention": (i32, [kvp, vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, f32,
+                                            vp, vp, sz, vp, vp]),
+        "vg_status_string": (ctypes.c_char_p, [i32]),
+        "vg_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(s: int) -> str:
+    return _lib.vg_status_string(int(s)).decode()
+
+
+def version() -> str:
+    return _lib.vg_version().decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise VGError(fn, status)
+
+
+@dataclass
+class PagedKV:
+    """Paged bf16 KV cache: pools [P][Hkv][16][d], page table [B][max_pages]."""
+    k_pages: torch.Tensor
+    v_pages: torch.Tensor
+    page_table: torch.Tensor
+
+    def __post_init__(self):
+        assert self.k_pages.dtype == torch.bfloat16 and self.v_pages.dtype == torch.bfloat16
+        assert self.k_pages.shape == self.v_pages.shape and self.k_pages.dim() == 4
+        assert self.page_table.dtype == torch.int32 and self.page_table.dim() == 2
+        assert self.k_pages.is_contiguous() and self.v_pages.is_contiguous()
+        assert self.page_table.is_contiguous()
+
+    @property
+    def num_kv_heads(self):
+        return self.k_pages.shape[1]
+
+    @property
+    def head_dim(self):
+        return self.k_pages.shape[3]
+
+    def struct(self) -> PagedKVStruct:
+        P, H, S, D = self.k_pages.shape
+        return PagedKVStruct(self.k_pages.data_ptr(), self.v_pages.data_ptr(),
+                             self.page_table.data_ptr(), P, S, self.page_table.shape[1], H, D)
+
+
+# --------------------------------------------------------------------- verify
+def verify_workspace_bytes(batch, n_rows, num_q_heads, num_kv_heads, head_dim, max_prefix,
+                           num_splits=0) -> int:
+    return int(_lib.vg_verify_workspace_bytes(batch, n_rows, num_q_heads, num_kv_heads, head_dim,
+                                              max_prefix, num_splits))
+
+
+def verify_attention(kv: PagedKV, q, prefix_lens, max_prefix, softmax_scale, out,
+                     capture_mode=CAPTURE_GROUP_SUM, capture=None, num_splits=0, workspace=None,
+                     error_flag=None, stream=None):
+    """vg_verify_attention.  q [B][R][Hq][d] bf16, prefix_lens int32 [B]."""
+    B, R, Hq, _ = q.shape
+    st = kv.struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = _lib.vg_verify_attention(ctypes.byref(st), _ptr(q), _ptr(prefix_lens), B, R, Hq,
+                                 int(max_prefix), float(softmax_scale), _ptr(out),
+                                 int(capture_mode), _ptr(capture), int(num_splits),
+                                 _ptr(workspace), ws_bytes, _ptr(error_flag), _stream(stream))
+    _check("vg_verify_attention", s)
+    return out
+
+
+# --------------------------------------------------------------------- select
+def select_kv(capture, capture_mode, prefix_lens, num_q_heads, num_kv_heads, max_prefix, top_k,
+              n_sink, n_recent, per_head, indices, counts, error_flag=None, stream=None):
+    """vg_select_kv.  indices int32 [B][rows][cap], counts int32 [B][rows]."""
+    B = prefix_lens.shape[0]
+    cap = indices.shape[-1]
+    s = _lib.vg_select_kv(_ptr(capture), int(capture_mode), _ptr(prefix_lens), B, num_q_heads,
+                          num_kv_heads, int(max_prefix), int(top_k), int(n_sink), int(n_recent),
+                          int(bool(per_head)), _ptr(indices), _ptr(counts), cap, None, 0,
+                          _ptr(error_flag), _stream(stream))
+    _check("vg_select_kv", s)
+    return indices, counts
+
+
+# ---------------------------------------------------------------- sparse draft
+def sparse_draft_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, cap, max_tail) -> int:
+    return int(_lib.vg_sparse_draft_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                    cap, max_tail))
+
+
+def sparse_draft_attention(kv: PagedKV, q, indices, counts, per_head, tail_start, cur_len,
+                           max_tail, softmax_scale, out, workspace=None, error_flag=None,
+                           stream=None):
+    """vg_sparse_draft_attention.  q [B][Hq][d] bf16."""
+    B, Hq, _ = q.shape
+    st = kv.struct()
+    cap = indices.shape[-1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = _lib.vg_sparse_draft_attention(ctypes.byref(st), _ptr(q), _ptr(indices), _ptr(counts),
+                                       int(bool(per_head)), cap, _ptr(tail_start), _ptr(cur_len),
+                                       B, Hq, int(max_tail), float(softmax_scale), _ptr(out),
+                                       _ptr(workspace), ws_bytes, _ptr(error_flag),
+                                       _stream(stream))
+    _check("vg_sparse_draft_attention", s)
+    return out
+
+
+def zero_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled byte workspace (the counters inside must start at zero)."""
+    return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)

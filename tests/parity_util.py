@@ -1,0 +1,146 @@
+"""Helpers for GPU-vs-oracle parity checks.
+
+Tolerances (bf16 inputs/outputs, fp32 accumulation on the GPU, float64 oracle):
+  attention outputs   max |gpu - oracle| <= 2e-2 and mean |gpu - oracle| <= 2e-3
+  captured logits     |gpu - oracle| <= 1e-3 * max(1, |oracle|)
+  index sets          bit-exact against the oracle's fp32 mirror fed the same
+                      captured tensor; against the float64 oracle end to end, a
+                      position may differ only if its oracle score lies within
+                      1e-4 (absolute, on the summed score) of the oracle's
+                      top_k-th candidate score.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import vg_oracle as O
+
+OUT_MAX, OUT_MEAN = 2e-2, 2e-3
+CAP_REL = 1e-3
+GAP = 1e-4
+
+
+def dense64(inp):
+    q = inp.q_verify.double().numpy()
+    k = [x.double().numpy() for x in inp.k_dense]
+    v = [x.double().numpy() for x in inp.v_dense]
+    return q, k, v
+
+
+def assert_close_out(got, ref, what=""):
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    assert err.max() <= OUT_MAX, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= OUT_MEAN, f"{what}: mean abs err {err.mean():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def assert_close_capture(got, ref, what=""):
+    got = np.asarray(got, np.float64)
+    bad = np.abs(got - ref) > CAP_REL * np.maximum(1.0, np.abs(ref))
+    assert not bad.any(), f"{what}: {bad.sum()} captured logits out of tolerance, e.g. " \
+                          f"{got[bad][:3]} vs {ref[bad][:3]}"
+
+
+def sub_problem(q, k, v, b, h, g):
+    """The verify inputs of one (sequence, KV head): Hq = g, Hkv = 1."""
+    return q[b:b + 1, :, h * g:(h + 1) * g], [k[b][h:h + 1]], [v[b][h:h + 1]]
+
+
+def check_verify(st, inp, pairs=None):
+    """Outputs of verify for the (b, kv head) pairs (all if None)."""
+    s = inp.spec
+    q, k, v = dense64(inp)
+    g = s.group
+    got = st.out_verify.float().cpu().numpy()
+    pairs = pairs or [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
+    for b, h in pairs:
+        qs, ks, vs = sub_problem(q, k, v, b, h, g)
+        out, rows = O.verify_attention(qs, ks, vs, [s.prefix_lens[b]], s.softmax_scale)
+        assert_close_out(got[b, :, h * g:(h + 1) * g], out[0], f"verify b={b} h={h}")
+
+
+def oracle_rows(inp):
+    q, k, _ = dense64(inp)
+    return O.capture_rows(q, k, inp.spec.prefix_lens, inp.spec.softmax_scale)
+
+
+def check_capture(st, inp, rows64):
+    s = inp.spec
+    cap = st.capture.cpu().numpy()
+    if st.capture_mode == O.CAPTURE_ROWS:
+        for b, L in enumerate(s.prefix_lens):
+            assert_close_capture(cap[b, :, :, :L], rows64[b, :, :, :L], f"rows b={b}")
+    else:
+        G = O.group_sum(rows64, s.num_kv_heads)
+        for b, L in enumerate(s.prefix_lens):
+            assert_close_capture(cap[b, :, :L], G[b, :, :L], f"group sum b={b}")
+
+
+def gpu_sets(st):
+    idx, cnt = st.indices.cpu().numpy(), st.counts.cpu().numpy()
+    B, rows, cap = idx.shape
+    sets = []
+    for b in range(B):
+        sets.append([idx[b, r, :cnt[b, r]] for r in range(rows)])
+        for r in range(rows):
+            assert (idx[b, r, cnt[b, r]:] == -1).all(), "padding must be -1"
+    return sets
+
+
+def check_select_mirror(st, inp):
+    """Bit-exact against the oracle's fp32 mirror on the GPU's own capture."""
+    s = inp.spec
+    cap = st.capture.cpu().numpy()
+    ref = O.select_kv(cap, st.capture_mode, s.prefix_lens, s.num_q_heads, s.num_kv_heads, s.top_k,
+                      s.n_sink, s.n_recent, st.per_head, mirror=True)
+    got = gpu_sets(st)
+    for b in range(s.batch):
+        for r in range(len(ref[b])):
+            assert got[b][r].tolist() == ref[b][r].tolist(), f"select b={b} row={r}"
+    return ref
+
+
+def check_select_end_to_end(st, inp, rows64):
+    """GPU capture -> GPU select vs float64 oracle capture -> float64 select."""
+    s = inp.spec
+    sc = O.selection_scores(rows64, O.CAPTURE_ROWS, s.num_q_heads, s.num_kv_heads, st.per_head)
+    ref = O.select_kv(rows64, O.CAPTURE_ROWS, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
+                      s.top_k, s.n_sink, s.n_recent, st.per_head)
+    got = gpu_sets(st)
+    worst = 0.0
+    for b, L in enumerate(s.prefix_lens):
+        for r in range(len(ref[b])):
+            a, o = set(got[b][r].tolist()), set(ref[b][r].tolist())
+            if a == o:
+                continue
+            cand = np.arange(s.n_sink, L - s.n_recent)
+            order = np.lexsort((cand, -sc[b, r, cand]))
+            kth = sc[b, r, cand[order[s.top_k - 1]]]
+            for pos in a ^ o:
+                gap = abs(sc[b, r, pos] - kth)
+                worst = max(worst, gap)
+                assert gap < GAP, f"b={b} row={r} pos={pos}: score gap {gap:.3e} to the k-th"
+    return worst
+
+
+def check_drafts(st, inp, sets, pairs=None, steps=None):
+    s = inp.spec
+    _, k, v = dense64(inp)
+    g = s.group
+    steps = steps or list(range(1, s.n_drafts + 1))
+    pairs = pairs or [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
+    for t in steps:
+        dq = inp.draft_q[t - 1].double().numpy()
+        got = st.out_draft[t - 1].float().cpu().numpy()
+        for b, h in pairs:
+            sel = [[sets[b][h if st.per_head else 0]]]
+            ref = O.sparse_draft_attention(dq[b:b + 1, h * g:(h + 1) * g], [k[b][h:h + 1]],
+                                           [v[b][h:h + 1]], sel, False, [s.prefix_lens[b]],
+                                           [s.prefix_lens[b] + t], s.softmax_scale)
+            assert_close_out(got[b, h * g:(h + 1) * g], ref[0], f"draft t={t} b={b} h={h}")
+
+
+def flag(st):
+    torch.cuda.synchronize()
+    return int(st.error_flag.item())

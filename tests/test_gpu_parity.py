@@ -1,0 +1,185 @@
+"""GPU kernels (through the C ABI) against the float64 oracle."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+from tests import parity_util as P
+
+pytestmark = pytest.mark.gpu
+
+vg = pytest.importorskip("self_speculative_sparse_vg_gb300.vg") if torch.cuda.is_available() else None
+
+
+def _require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+
+
+def _run(spec, capture_mode=1, per_head=None, num_splits=0):
+    from self_speculative_sparse_vg_gb300.step import DecodeStep
+    from self_speculative_sparse_vg_gb300.workloads import make_inputs
+    inp = make_inputs(spec)
+    st = DecodeStep.create(inp, "cuda", capture_mode=capture_mode, per_head=per_head,
+                           num_splits=num_splits)
+    st.run()
+    assert P.flag(st) == 0
+    return inp, st
+
+
+SMALL = dict(
+    base={},
+    d64=dict(head_dim=64),
+    mha=dict(num_q_heads=4, num_kv_heads=4),
+    g8=dict(num_q_heads=16, num_kv_heads=2),
+    g5=dict(num_q_heads=10, num_kv_heads=2, n_drafts=7),
+    k0=dict(n_drafts=0),
+    k1=dict(n_drafts=1),
+    pages_shuffled=dict(shuffle_pages=True, extra_pages=5),
+    short=dict(prefix_lens=(1, 15, 16, 63, 64, 65, 130), batch=7, top_k=8, n_sink=2, n_recent=4),
+    budget_all=dict(prefix_lens=(40, 83), top_k=64, n_sink=4, n_recent=16),
+    ties=dict(prefix_lens=(700,), batch=1, top_k=33),
+)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("mode,per_head", [(1, False), (2, False), (1, True), (2, True)])
+def test_small_step(name, mode, per_head):
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    spec = small_spec(**SMALL[name])
+    inp, st = _run(spec, capture_mode=mode, per_head=per_head)
+    P.check_verify(st, inp)
+    rows64 = P.oracle_rows(inp)
+    P.check_capture(st, inp, rows64)
+    sets = P.check_select_mirror(st, inp)
+    P.check_select_end_to_end(st, inp, rows64)
+    P.check_drafts(st, inp, sets)
+
+
+def test_ties_select_lower_position():
+    """All-equal captured scores: the kept candidates are the lowest positions."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300 import vg as V
+    B, Hq, Hkv, L = 1, 8, 2, 3000
+    cap = torch.ones(B, Hkv, L, device="cuda")
+    cap[0, :, 2000:2010] = 5.0
+    lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    idx = torch.full((B, 1, 4 + 16 + 100), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(B, 1, dtype=torch.int32, device="cuda")
+    V.select_kv(cap, V.CAPTURE_GROUP_SUM, lens, Hq, Hkv, L, 100, 4, 16, False, idx, cnt)
+    torch.cuda.synchronize()
+    want = list(range(4)) + list(range(4, 94)) + list(range(2000, 2010)) + list(range(L - 16, L))
+    assert idx[0, 0].tolist() == sorted(want)
+    assert cnt.item() == 120
+
+
+def test_split_count_invariance():
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    spec = small_spec(prefix_lens=(3000, 1777))
+    outs, caps = [], []
+    for ns in (1, 2, 7, 0):
+        inp, st = _run(spec, num_splits=ns)
+        outs.append(st.out_verify.float().cpu())
+        caps.append(st.capture.cpu())
+        P.check_verify(st, inp)
+    for o, c in zip(outs[1:], caps[1:]):
+        assert (o - outs[0]).abs().max().item() <= 1e-2
+        assert torch.equal(c, caps[0])          # logits do not depend on the split
+
+
+def test_group_sum_equals_mirror_of_rows():
+    """Mode A written by the kernel == fp32 mirror sum of the mode-B rows."""
+    _require_gpu()
+    from oracle import vg_oracle as O
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    spec = small_spec(num_q_heads=10, num_kv_heads=2)
+    _, a = _run(spec, capture_mode=1)
+    _, bb = _run(spec, capture_mode=2)
+    G = O.group_sum_mirror(bb.capture.cpu().numpy(), spec.num_kv_heads)
+    for b, L in enumerate(spec.prefix_lens):
+        np.testing.assert_array_equal(a.capture.cpu().numpy()[b, :, :L], G[b, :, :L])
+
+
+def test_poisoned_workspace_and_repeat():
+    """Partials must be written before they are read: NaN-filled partials and
+    back-to-back calls on one workspace give the same result."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.step import DecodeStep
+    from self_speculative_sparse_vg_gb300.workloads import make_inputs, small_spec
+    inp = make_inputs(small_spec(prefix_lens=(2500, 900)))
+    st = DecodeStep.create(inp, "cuda", num_splits=5)
+    st.run()
+    ref_v, ref_d = st.out_verify.clone(), st.out_draft.clone()
+    wsv = st.ws_verify.view(torch.uint8)
+    n_tick = 256
+    wsv[:-n_tick].view(torch.uint8).fill_(0xFF)   # NaN bit patterns in the partials
+    wsd = st.ws_draft.view(torch.uint8)
+    wsd[:-n_tick].fill_(0xFF)
+    for _ in range(3):
+        st.run()
+    assert P.flag(st) == 0
+    assert torch.equal(st.out_verify, ref_v)
+    assert torch.equal(st.out_draft, ref_d)
+
+
+def test_device_errors_flag_and_skip():
+    """Bad page ids, indices, counts and lengths set the error flag; the
+    offending load is skipped (no fault)."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300 import vg as V
+    from self_speculative_sparse_vg_gb300.step import DecodeStep
+    from self_speculative_sparse_vg_gb300.workloads import make_inputs, small_spec
+    inp = make_inputs(small_spec())
+    st = DecodeStep.create(inp, "cuda")
+    st.kv.page_table[0, 3] = st.kv.k_pages.shape[0] + 5       # out-of-range page id
+    st.verify()
+    assert P.flag(st) & V.DEVERR_PAGE
+    st.error_flag.zero_()
+    st.kv.page_table.copy_(inp.page_table.cuda())
+    st.run()
+    assert P.flag(st) == 0
+    st.indices[0, 0, 0] = int(st.prefix_lens[0]) + 3          # index beyond the prefix
+    st.draft(1)
+    assert P.flag(st) & V.DEVERR_INDEX
+    st.error_flag.zero_()
+    st.counts[1, 0] = st.indices.shape[-1] + 1                # count above cap
+    st.draft(1)
+    assert P.flag(st) & V.DEVERR_COUNT
+    st.error_flag.zero_()
+    st.prefix_lens[1] = st.spec.max_prefix + 1               # length above the host bound
+    st.verify()
+    st.select()
+    assert P.flag(st) & V.DEVERR_LENGTH
+
+
+FULL = ["tiny_d64_2k", "llama8b_32k", "llama8b_b8_16k_64k", "qwen14b_128k"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    """Full-size workloads in the launch configuration the benchmark uses:
+    sampled (sequence, KV head) pairs for attention, every selection row
+    bit-exact against the mirror, end-to-end selection within the gap rule."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.workloads import WORKLOADS
+    spec = WORKLOADS[name]
+    modes = [(1, False), (2, True)] if spec.batch > 1 else [(1, False)]
+    for mode, per_head in modes:
+        inp, st = _run(spec, capture_mode=mode, per_head=per_head)
+        if name == "tiny_d64_2k":
+            pairs = None
+        else:
+            pairs = [(0, 0), (spec.batch - 1, spec.num_kv_heads - 1)]
+        P.check_verify(st, inp, pairs)
+        rows64 = P.oracle_rows(inp)
+        P.check_capture(st, inp, rows64)
+        sets = P.check_select_mirror(st, inp)
+        P.check_select_end_to_end(st, inp, rows64)
+        P.check_drafts(st, inp, sets, pairs=pairs, steps=[1, spec.n_drafts])
+        if name == "tiny_d64_2k":
+            assert set(inp.planted[0].tolist()) <= set(sets[0][0].tolist())
+        del st
+        torch.cuda.empty_cache()

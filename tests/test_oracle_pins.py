@@ -316,3 +316,10 @@ def test_paging_round_trip():
         recv = inp.v_pages[ids].permute(1, 0, 2, 3).reshape(kd.shape[0], npg * 16, -1)[:, :n]
         assert (recv == inp.v_dense[b]).all()
         assert (inp.page_table[b, npg:] == -1).all()
+
+
+def test_capture_rows_equals_verify_capture():
+    rng = np.random.default_rng(31)
+    q, k, v = _rand_case(rng, 2, 4, 8, 2, 16, [19, 6])
+    _, rows = O.verify_attention(q, k, v, [19, 6], 0.2)
+    np.testing.assert_allclose(O.capture_rows(q, k, [19, 6], 0.2), rows, rtol=0, atol=1e-12)
