@@ -145,10 +145,15 @@ __global__ void __launch_bounds__(kDraftThreads)
   cp_async_wait<1>();
   __syncthreads();
 
-  // logits: row slot = warp * RPW + lane / LPR
+  // logits: row slot = warp * RPW + lane / LPR.  The trip count is uniform
+  // across the warp (rows past ne are predicated off) because the loop body
+  // shuffles with a full mask.
   const int slot = warp * RPW + lane / LPR;
-  for (int e = slot; e < ne; e += SLOTS) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(&kv_s[0][e][ch * 8]);
+  for (int base = warp * RPW; base < ne; base += SLOTS) {
+    const int e = base + lane / LPR;
+    const bool ev = e < ne;
+    const uint4 raw = ev ? *reinterpret_cast<const uint4*>(&kv_s[0][e][ch * 8])
+                         : make_uint4(0, 0, 0, 0);
     const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
     float kf[8];
 #pragma unroll
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(kDraftThreads)
     for (int o = LPR / 2; o > 0; o >>= 1)
 #pragma unroll
       for (int qi = 0; qi < GMAX; ++qi) dot[qi] += __shfl_xor_sync(0xffffffffu, dot[qi], o);
-    if (ch == 0) {
+    if (ev && ch == 0) {
       const bool valid = off_s[e] >= 0;
 #pragma unroll
       for (int qi = 0; qi < GMAX; ++qi)
