@@ -187,6 +187,38 @@ vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void* q, const 
                                     void* workspace, size_t workspace_bytes,
                                     int32_t* error_flag, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Allocation-free verification attention.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory --
+ * for example an inference runtime that owns every byte of HBM through its
+ * own pool and forbids libraries from calling cudaMalloc, or a decode loop
+ * that must not call an allocator because cudaMalloc/cudaFree can
+ * synchronise the device.  It computes exactly what vg_verify_attention
+ * computes (same arguments minus the workspace) and allocates nothing.
+ *
+ * Its split-K scratch is one fixed device array of
+ * vg_verify_noalloc_scratch_bytes() bytes (16 MiB), held by every GPU that
+ * loads the library until the process exits.  Shapes needing more scratch
+ * than that (vg_verify_workspace_bytes() above it) are rejected with
+ * VG_ERR_WORKSPACE_TOO_SMALL before anything is launched; use
+ * vg_verify_attention with a caller workspace for those.
+ *
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call shares the one array.  Each call clears the merge counters
+ *     it uses (a cudaMemsetAsync on `stream`); two calls that overlap on the
+ *     GPU (different streams, no ordering between them) race on it.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ * ------------------------------------------------------------------------- */
+size_t vg_verify_noalloc_scratch_bytes(void);
+
+vg_status vg_verify_attention_noalloc(const vg_paged_kv* kv, const void* q,
+                                      const int32_t* prefix_lens, int batch, int n_rows,
+                                      int num_q_heads, int max_prefix, float softmax_scale,
+                                      void* out, int capture_mode, float* capture,
+                                      int num_splits, int32_t* error_flag, cudaStream_t stream);
+
 /* Static string for a status code (host). */
 const char* vg_status_string(vg_status status);
 

@@ -21,6 +21,8 @@
 //    sum in a fixed order, with coalesced stores.
 //  * Splits over the KV length are merged by the last CTA of each
 //    (sequence, KV head) to finish (atomic ticket, no waiting).
+#include <mutex>
+
 #include "vg_device.cuh"
 #include "vg_host.h"
 
@@ -622,4 +624,67 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
     e = pl.pg == 4 ? launch_verify<64, 4>(pl, tk, tv, p, grid, stream)
                    : launch_verify<64, 2>(pl, tk, tv, p, grid, stream);
   return e == cudaSuccess ? VG_OK : VG_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of vg_verify_attention (declared in vg.h).
+//
+// Its split partials and merge tickets live in one file-scope device array of
+// fixed size instead of a caller-provided workspace.  The array exists once
+// per GPU that loads this library and stays resident until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) uint8_t g_verify_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+void* noalloc_scratch_on_current_device() {
+  static void* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_verify_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" size_t vg_verify_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" vg_status vg_verify_attention_noalloc(const vg_paged_kv* kv, const void* q,
+                                                 const int32_t* prefix_lens, int batch,
+                                                 int n_rows, int num_q_heads, int max_prefix,
+                                                 float softmax_scale, void* out,
+                                                 int capture_mode, float* capture,
+                                                 int num_splits, int32_t* error_flag,
+                                                 cudaStream_t stream) {
+  vg_status st = check_paged_kv(kv);
+  if (st != VG_OK) return st;
+  if (batch <= 0 || n_rows <= 0 || num_q_heads <= 0 || max_prefix <= 0 || num_splits < 0 ||
+      num_q_heads % kv->num_kv_heads)
+    return VG_ERR_INVALID_ARGUMENT;
+  VerifyPlan pl;
+  if (!make_verify_plan(batch, n_rows, num_q_heads, kv->num_kv_heads, kv->head_dim, max_prefix,
+                        num_splits, &pl))
+    return VG_ERR_INVALID_ARGUMENT;
+  if (pl.ws_bytes > kNoAllocScratchBytes) return VG_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* scratch = static_cast<uint8_t*>(noalloc_scratch_on_current_device());
+  if (!scratch) return VG_ERR_LAUNCH;
+  if (pl.ws_bytes > 0) {
+    // The array keeps the previous call's contents: the merge tickets must
+    // start at zero, the partials are always written before they are read.
+    if (cudaMemsetAsync(scratch + pl.off_tickets, 0, (size_t)batch * kv->num_kv_heads * 4,
+                        stream) != cudaSuccess)
+      return VG_ERR_LAUNCH;
+  }
+  return vg_verify_attention(kv, q, prefix_lens, batch, n_rows, num_q_heads, max_prefix,
+                             softmax_scale, out, capture_mode, capture, num_splits, scratch,
+                             kNoAllocScratchBytes, error_flag, stream);
 }

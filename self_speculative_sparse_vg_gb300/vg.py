@@ -30,6 +30,7 @@ EXPORTED = (
     "vg_select_workspace_bytes", "vg_select_kv",
     "vg_sparse_draft_workspace_bytes", "vg_sparse_draft_attention",
     "vg_status_string", "vg_version",
+    "vg_verify_noalloc_scratch_bytes", "vg_verify_attention_noalloc",
 )
 
 
@@ -63,6 +64,9 @@ def _load():
         "vg_sparse_draft_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "vg_sparse_draft_attention": (i32, [kvp, vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, f32,
                                             vp, vp, sz, vp, vp]),
+        "vg_verify_noalloc_scratch_bytes": (sz, []),
+        "vg_verify_attention_noalloc": (i32, [kvp, vp, vp, i32, i32, i32, i32, f32, vp, i32, vp,
+                                              i32, vp, vp]),
         "vg_status_string": (ctypes.c_char_p, [i32]),
         "vg_version": (ctypes.c_char_p, []),
     }
@@ -145,6 +149,21 @@ def verify_attention(kv: PagedKV, q, prefix_lens, max_prefix, softmax_scale, out
                                  int(capture_mode), _ptr(capture), int(num_splits),
                                  _ptr(workspace), ws_bytes, _ptr(error_flag), _stream(stream))
     _check("vg_verify_attention", s)
+    return out
+
+
+def verify_attention_noalloc(kv: PagedKV, q, prefix_lens, max_prefix, softmax_scale, out,
+                             capture_mode=CAPTURE_GROUP_SUM, capture=None, num_splits=0,
+                             error_flag=None, stream=None):
+    """vg_verify_attention_noalloc: same result, scratch in the library's
+    fixed device array instead of a caller workspace."""
+    B, R, Hq, _ = q.shape
+    st = kv.struct()
+    s = _lib.vg_verify_attention_noalloc(ctypes.byref(st), _ptr(q), _ptr(prefix_lens), B, R, Hq,
+                                         int(max_prefix), float(softmax_scale), _ptr(out),
+                                         int(capture_mode), _ptr(capture), int(num_splits),
+                                         _ptr(error_flag), _stream(stream))
+    _check("vg_verify_attention_noalloc", s)
     return out
 
 
