@@ -29,10 +29,10 @@
  *     VG_DEVERR_* bit into *error_flag (when error_flag is not NULL) and skip
  *     the offending load or sequence; nothing traps.
  *   - Workspaces: sized by the matching *_workspace_bytes() call for the same
- *     arguments on the same device.  A workspace must be zero-filled once
- *     before its first use; every completed call leaves it reusable (its
- *     counters return to zero).  Calls that share a workspace must not
- *     overlap in time.
+ *     arguments on the same device (0 = none needed, the pointer may be
+ *     NULL).  They need no initialisation: everything in them is written
+ *     before it is read.  Calls that share a workspace must not overlap in
+ *     time.
  */
 #ifndef VG_H_
 #define VG_H_
@@ -113,7 +113,9 @@ typedef struct vg_paged_kv {
  *                NULL with VG_CAPTURE_NONE.
  *   num_splits   0 = automatic; otherwise the number of KV-length splits
  *                (clamped to the number of 64-position tiles).  Results agree
- *                across split counts up to float32 rounding.
+ *                across split counts up to float32 rounding.  With more than
+ *                one split, the call launches a second, small merge kernel
+ *                (programmatic dependent launch) on the same stream.
  * Supported: head_dim 64/128, page_size 16, group g = num_q_heads /
  * num_kv_heads in [1, 8], g * n_rows <= 96, n_rows <= 16.
  * ------------------------------------------------------------------------- */
@@ -149,7 +151,7 @@ vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q, const int32_
  *   indices  int32 [batch][rows][cap], ascending, entries past the count = -1.
  *   counts   int32 [batch][rows].
  *   cap      >= min(max_prefix, n_sink + n_recent + top_k).
- * Supported: max_prefix <= 262144.
+ * Supported: max_prefix <= 262144, num_q_heads / num_kv_heads <= 8.
  * ------------------------------------------------------------------------- */
 size_t vg_select_workspace_bytes(int batch, int num_kv_heads, int max_prefix, int per_head);
 
@@ -174,8 +176,10 @@ vg_status vg_select_kv(const float* capture, int capture_mode, const int32_t* pr
  *               cur_len), 0 <= cur_len - tail_start <= max_tail.
  *   out         bf16 [batch][num_q_heads][head_dim].
  * The attended list (selection, then tail) is processed in chunks of 64
- * entries, one CTA each, merged by the last CTA to finish.
- * Supported: head_dim 64/128, g in [1, 8].
+ * entries by one thread-block cluster per (sequence, KV head), merged in
+ * distributed shared memory; no workspace is needed
+ * (vg_sparse_draft_workspace_bytes returns 0; workspace may be NULL).
+ * Supported: head_dim 64/128, g in [1, 8], cap + max_tail <= 8192.
  * ------------------------------------------------------------------------- */
 size_t vg_sparse_draft_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
                                        int head_dim, int cap, int max_tail);
@@ -206,8 +210,8 @@ vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void* q, const 
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
- *   - Every call shares the one array.  Each call clears the merge counters
- *     it uses (a cudaMemsetAsync on `stream`); two calls that overlap on the
+ *   - Every call shares the one array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero); two calls that overlap on the
  *     GPU (different streams, no ordering between them) race on it.
  *   - No cudaMalloc, cudaFree or allocating library routine is called.
  * ------------------------------------------------------------------------- */

@@ -50,27 +50,41 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 }
 
 // Score of prefix position j for selection row `row` of sequence b, summed in
-// the order documented in vg.h (plain fp32 adds, no reassociation).
+// the order documented in vg.h (plain fp32 adds, no reassociation).  The loads
+// of one position are all issued before the first add (batches of 16), so a
+// score costs one memory round trip per batch rather than one per term.
+constexpr int kLoadBatch = 16;
+
 __device__ __forceinline__ float row_score(const SelectParams& p, int b, int row, int j) {
   const size_t L = p.max_prefix;
   if (p.capture_mode == VG_CAPTURE_GROUP_SUM) {
     const float* G = p.capture + (size_t)b * p.num_kv_heads * L + j;
     if (p.per_head) return __ldg(G + (size_t)row * L);
-    float acc = __ldg(G);
-    for (int h = 1; h < p.num_kv_heads; ++h) acc = acc + __ldg(G + (size_t)h * L);
+    float acc = 0.f;
+    for (int h0 = 0; h0 < p.num_kv_heads; h0 += kLoadBatch) {
+      float v[kLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u)
+        v[u] = (h0 + u < p.num_kv_heads) ? __ldg(G + (size_t)(h0 + u) * L) : 0.f;
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u)
+        if (h0 + u < p.num_kv_heads) acc = (h0 + u == 0) ? v[u] : acc + v[u];
+    }
     return acc;
   }
   const float* Rw = p.capture + (size_t)b * p.num_q_heads * 2 * L + j;  // [q][2][L]
-  const int g = p.group;
+  const int g = p.group;  // <= 8, so one KV head's 2g terms fit one batch
   const int h0 = p.per_head ? row : 0, h1 = p.per_head ? row + 1 : p.num_kv_heads;
   float acc = 0.f;
   for (int h = h0; h < h1; ++h) {
-    const int q0 = h * g;
-    float G = __ldg(Rw + (size_t)(2 * q0) * L) + __ldg(Rw + (size_t)(2 * q0 + 1) * L);
-    for (int qi = 1; qi < g; ++qi) {
-      const int q = q0 + qi;
-      G = G + (__ldg(Rw + (size_t)(2 * q) * L) + __ldg(Rw + (size_t)(2 * q + 1) * L));
-    }
+    float v[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      v[u] = (u < 2 * g) ? __ldg(Rw + (size_t)(2 * h * g + u) * L) : 0.f;
+    float G = v[0] + v[1];
+#pragma unroll
+    for (int qi = 1; qi < kLoadBatch / 2; ++qi)
+      if (qi < g) G = G + (v[2 * qi] + v[2 * qi + 1]);
     acc = (h == h0) ? G : acc + G;
   }
   return acc;
@@ -134,6 +148,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   }
   const int c_lo = p.n_sink, c_hi = L - p.n_recent;  // candidates [c_lo, c_hi)
 
+#pragma unroll 4
   for (int j = tid; j < n_loc; j += blockDim.x) keys[j] = score_key(row_score(p, b, row, lo + j));
   __syncthreads();
 
@@ -158,9 +173,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
         if (v && lane == __ffs(grp) - 1) atomicAdd(&hb[dig], (uint32_t)__popc(grp));
       }
       cluster.sync();
-      if (tid < 256) {
+      if (tid < 256) {  // all C remote loads issued before any is used
+        uint32_t v[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) v[c] = c < C ? cluster.map_shared_rank(hb, c)[tid] : 0u;
         uint32_t t = 0;
-        for (int c = 0; c < C; ++c) t += cluster.map_shared_rank(hb, c)[tid];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c) t += v[c];
         tot_s[tid] = t;
       }
       __syncthreads();
@@ -217,15 +236,22 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
     }
   }
   cluster.sync();
-  if (tid == 0) {
-    int gb = 0, eb = 0;
-    for (int c = 0; c < rank; ++c) {
-      const int* rc = cluster.map_shared_rank(cnt, c);
-      gb += rc[0];
-      eb += rc[1];
+  if (tid < 32) {  // lane c reads CTA c's counts; sum over the lower ranks
+    int gv = 0, ev = 0;
+    if (lane < rank) {
+      const int* rc = cluster.map_shared_rank(cnt, lane);
+      gv = rc[0];
+      ev = rc[1];
     }
-    ctl[2] = gb;
-    ctl[3] = eb;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gv += __shfl_xor_sync(0xffffffffu, gv, o);
+      ev += __shfl_xor_sync(0xffffffffu, ev, o);
+    }
+    if (lane == 0) {
+      ctl[2] = gv;
+      ctl[3] = ev;
+    }
   }
   cluster.sync();  // no CTA leaves while another may still read its shared memory
 
@@ -288,6 +314,7 @@ extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
   if (capture_mode != VG_CAPTURE_GROUP_SUM && capture_mode != VG_CAPTURE_ROWS)
     return VG_ERR_INVALID_ARGUMENT;
   if (num_q_heads % num_kv_heads) return VG_ERR_INVALID_ARGUMENT;
+  if (num_q_heads / num_kv_heads > 8) return VG_ERR_UNSUPPORTED;
   const long long budget = (long long)n_sink + n_recent + top_k;
   if (cap < std::min<long long>(max_prefix, budget)) return VG_ERR_INVALID_ARGUMENT;
   int C, slice;

@@ -14,13 +14,17 @@
 //  * A producer warp streams 64-position tiles (4 pages) of K and V into a
 //    shared-memory ring with 4-D TMA loads (128-byte swizzle, evict-first
 //    L2 policy); consumers wait on mbarriers (bounded waits).
-//  * Consumer warp (mt, pg) owns rows [16 mt, 16 mt + 16) and a 64/PG
-//    position slice of every tile; it keeps its own online-softmax state.
-//  * Capture epilogue: the first-tile warps stage their 16 x (64/PG) logits
+//  * Consumer warp (mt, grp) owns rows [16 mt, 16 mt + 16) of whole 64-position
+//    tiles; the NG warp groups take alternating tiles, each keeping its own
+//    online-softmax state (8 independent MMA accumulators per warp, softmax
+//    reductions and rescales amortised over 64 positions).
+//  * Capture epilogue: the first-row-tile warps stage their 16 x 64 logits
 //    in shared memory and write either the raw two rows or their per-KV-head
 //    sum in a fixed order, with coalesced stores.
-//  * Splits over the KV length are merged by the last CTA of each
-//    (sequence, KV head) to finish (atomic ticket, no waiting).
+//  * Splits over the KV length write fp32 partials (O, m, l) to the
+//    workspace; a small merge kernel, one CTA per (output row, KV head,
+//    sequence), combines them.  It is chained with programmatic dependent
+//    launch, so its launch overlaps the verify grid.
 #include <mutex>
 
 #include "vg_device.cuh"
@@ -40,11 +44,10 @@ struct VerifyParams {
   float* capture;
   float* part_o;      // [B][Hkv][splits][M][HD]
   float* part_ml;     // [B][Hkv][splits][M][2]
-  int32_t* tickets;   // [B][Hkv]
   int32_t* error_flag;
   int batch, n_rows, num_q_heads, num_kv_heads, group, m_rows, m_tiles;
   int max_prefix, max_pages_per_seq, num_pages;
-  int capture_mode, splits, tiles_per_split, stages;
+  int capture_mode, splits, tiles_per_split, stages, groups;
   float scale, scale_log2;
 };
 
@@ -70,24 +73,19 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t v, int pos, int n) {
   return v;
 }
 
-template <int HD>
-struct VerifyLayout {
-  static constexpr int kTileBytes = kTileN * HD * 2;     // one of K / V
-  static constexpr int kStageBytes = 2 * kTileBytes;
-};
+constexpr int kVerifyMaxThreads = 256;  // <= 7 consumer warps + 1 producer
 
-template <int HD, int PG>
-__global__ void __launch_bounds__(416, 1)
+template <int HD>
+__global__ void __launch_bounds__(kVerifyMaxThreads, 1)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const VerifyParams p) {
-  constexpr int NPW = kTileN / PG;  // positions per warp per tile
-  constexpr int NT = NPW / 8;       // S n-tiles per warp
-  constexpr int KS = HD / 16;       // k-steps of Q K^T
-  constexpr int DN = HD / 8;        // O n-tiles
-  constexpr int CH = HD / 8;        // 16-byte chunks per row
-  constexpr int kTileBytes = VerifyLayout<HD>::kTileBytes;
-  constexpr int kStageBytes = VerifyLayout<HD>::kStageBytes;
-  constexpr int kCapCols = 32;
+  constexpr int NT = kTileN / 8;  // S n-tiles per warp: a warp owns a whole 64-position tile
+  constexpr int KS = HD / 16;     // k-steps of Q K^T
+  constexpr int DN = HD / 8;      // O n-tiles
+  constexpr int CH = HD / 8;      // 16-byte chunks per row
+  constexpr int kTileBytes = kTileN * HD * 2;  // one of K / V
+  constexpr int kStageBytes = 2 * kTileBytes;
+  constexpr int kCapStride = 72;  // floats per row of a warp's capture staging tile
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -95,16 +93,16 @@ __global__ void __launch_bounds__(416, 1)
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.group, R = p.n_rows, M = p.m_rows;
-  const int n_cons = p.m_tiles * PG;
-  const int Mpad = p.m_tiles * 16;
+  const int MT = p.m_tiles, NG = p.groups;
+  const int n_cons = MT * NG;
+  const int Mpad = MT * 16;
   const int stages = p.stages;
 
   uint8_t* ring = smem;
   uint8_t* qs = ring + stages * kStageBytes;
   float* cbuf = reinterpret_cast<float*>(qs + Mpad * HD * 2);
-  uint64_t* full = reinterpret_cast<uint64_t*>(cbuf + PG * 16 * kCapCols);
+  uint64_t* full = reinterpret_cast<uint64_t*>(cbuf + NG * 16 * kCapStride);
   uint64_t* empty = full + stages;
-  int* s_flag = reinterpret_cast<int*>(empty + stages);
 
   const int L = p.prefix_lens[b];
   const int n_b = L + R;
@@ -120,23 +118,11 @@ __global__ void __launch_bounds__(416, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], n_cons);
+      mbar_init(&empty[s], MT);  // a tile is consumed by the MT warps of one group
     }
     fence_barrier_init();
   }
-  // Q rows of this KV head -> shared (same swizzled layout as K), padding zero.
-  for (int idx = threadIdx.x; idx < Mpad * CH; idx += blockDim.x) {
-    const int row = idx / CH, ch = idx - (idx / CH) * CH;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < M) {
-      int i, qi;
-      row_of(row, g, R, i, qi);
-      const size_t off = ((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD + ch * 8;
-      v = *reinterpret_cast<const uint4*>(p.q + off);
-    }
-    *reinterpret_cast<uint4*>(qs + sw128_offset(row, ch, Mpad)) = v;
-  }
-  __syncthreads();
+  __syncthreads();  // barriers initialised: the producer may start at once
 
   float mrun0 = -INFINITY, mrun1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float acc[DN][4];
@@ -145,42 +131,70 @@ __global__ void __launch_bounds__(416, 1)
 
   if (warp == n_cons) {
     // ---------------------------------------------------------- producer
-    if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
+    // The warp fetches the page ids of 8 tiles (32 ids, one per lane) in one
+    // round trip; lane 0 then issues the tiles' TMA loads as stages free up.
+    if (ntiles > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+      }
       const uint64_t pol = l2_policy_evict_first();
+      int my_id = p.num_pages;
       for (int lt = 0; lt < ntiles; ++lt) {
-        const int st = lt % stages;
-        if (lt >= stages && !mbar_wait(&empty[st], ((lt / stages) - 1) & 1)) {
-          flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-          break;
-        }
-        uint8_t* kt = ring + st * kStageBytes;
-        uint8_t* vt = kt + kTileBytes;
-        mbar_arrive_expect_tx(&full[st], kStageBytes);
-#pragma unroll
-        for (int pi = 0; pi < kTileN / kPageSize; ++pi) {
-          const int lp = (t0 + lt) * (kTileN / kPageSize) + pi;
-          int phys = p.num_pages;  // out of range: TMA fills zeros
-          if (lp < npages_b) {
+        if ((lt & 7) == 0) {
+          const int lt_l = lt + (lane >> 2);
+          const int lp = (t0 + lt_l) * (kTileN / kPageSize) + (lane & 3);
+          my_id = p.num_pages;  // out of range: TMA fills zeros
+          if (lt_l < ntiles && lp < npages_b) {
             const int e = p.page_table[(size_t)b * p.max_pages_per_seq + lp];
             if (e >= 0 && e < p.num_pages)
-              phys = e;
+              my_id = e;
             else
               flag_error(p.error_flag, VG_DEVERR_PAGE);
           }
-#pragma unroll
-          for (int dh = 0; dh < HD / 64; ++dh) {
-            const int off = dh * kTileN * 128 + pi * kPageSize * 128;
-            tma_load_4d(kt + off, &tmk, &full[st], dh * 64, 0, h, phys, pol);
-            tma_load_4d(vt + off, &tmv, &full[st], dh * 64, 0, h, phys, pol);
-          }
         }
+        const int st = lt % stages;
+        int go = 1;
+        if (lane == 0 && lt >= stages) go = mbar_wait(&empty[st], ((lt / stages) - 1) & 1);
+        go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) {
+          if (lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+          break;
+        }
+        // one TMA box (16 positions x 64 dims) per lane: page pi, half dh, K or V
+        constexpr int kBoxes = (kTileN / kPageSize) * (HD / 64) * 2;
+        const int pi = lane / ((HD / 64) * 2), dh = (lane >> 1) & (HD / 64 - 1), kv = lane & 1;
+        const int id = __shfl_sync(0xffffffffu, my_id, (lt & 7) * 4 + (pi & 3));
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], kStageBytes);
+        __syncwarp();
+        if (lane < kBoxes) {
+          uint8_t* dst = ring + st * kStageBytes + kv * kTileBytes + dh * kTileN * 128 +
+                         pi * kPageSize * 128;
+          tma_load_4d(dst, kv ? &tmv : &tmk, &full[st], dh * 64, 0, h, id, pol);
+        }
+        __syncwarp();
       }
     }
   } else {
     // ---------------------------------------------------------- consumers
-    const int mt = warp / PG, pg = warp - (warp / PG) * PG;
+    // Q rows of this KV head -> shared (same swizzled layout as K), padding
+    // zero; only the consumer warps wait for it (named barrier 1).
+    for (int idx = threadIdx.x; idx < Mpad * CH; idx += n_cons * 32) {
+      const int row = idx / CH, ch = idx - (idx / CH) * CH;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (row < M) {
+        int i, qi;
+        row_of(row, g, R, i, qi);
+        const size_t off = ((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD + ch * 8;
+        v = *reinterpret_cast<const uint4*>(p.q + off);
+      }
+      *reinterpret_cast<uint4*>(qs + sw128_offset(row, ch, Mpad)) = v;
+    }
+    named_barrier_sync(1, n_cons * 32);
+    // warp (mt, grp): rows [16 mt, 16 mt + 16) of tiles grp, grp + NG, ...
+    // The ring depth is a multiple of NG, so a stage's previous phase was
+    // consumed by this same group and a parity wait can never see it stale.
+    const int mt = warp % MT, grp = warp / MT;
     const int r = lane >> 2, c = lane & 3;
     const int m0 = mt * 16 + r, m1 = m0 + 8;
     int lim0 = n_b - 1, lim1 = n_b - 1;  // last attended position of each row
@@ -189,23 +203,22 @@ __global__ void __launch_bounds__(416, 1)
       if (m0 < M) { row_of(m0, g, R, i, qi); lim0 = L + i; }
       if (m1 < M) { row_of(m1, g, R, i, qi); lim1 = L + i; }
     }
-    // Q fragments: held in registers by the 4-slice variant; the 2-slice
-    // variant (many row tiles, more warps) re-reads them per tile instead.
-    constexpr bool kQReg = (PG == 4);
     const uint32_t qs_u = smem_u32(qs);
-    uint32_t qa[kQReg ? KS : 1][4];
+    uint32_t qa[KS][4];
     const int qrow = mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-    if (kQReg) {
 #pragma unroll
-      for (int ks = 0; ks < (kQReg ? KS : 1); ++ks)
-        ldsm_x4(qs_u + sw128_offset(qrow, 2 * ks + (lane >> 4), Mpad), qa[ks][0], qa[ks][1],
-                qa[ks][2], qa[ks][3]);
-    }
+    for (int ks = 0; ks < KS; ++ks)
+      ldsm_x4(qs_u + sw128_offset(qrow, 2 * ks + (lane >> 4), Mpad), qa[ks][0], qa[ks][1],
+              qa[ks][2], qa[ks][3]);
     const bool cap_warp = (mt == 0) && (p.capture_mode != VG_CAPTURE_NONE);
-    float* cb = cbuf + pg * 16 * kCapCols;
+    float* cb = cbuf + grp * 16 * kCapStride;
     const uint32_t ring_u = smem_u32(ring);
+    const int krow = (lane & 7) + ((lane >> 4) << 3);       // K ldmatrix row within 16
+    const int kchk = (lane >> 3) & 1;                        // K ldmatrix chunk offset
+    const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3);  // V ldmatrix.trans row within 16
+    const int vchk = lane >> 4;                              // V ldmatrix.trans chunk offset
 
-    for (int lt = 0; lt < ntiles; ++lt) {
+    for (int lt = grp; lt < ntiles; lt += NG) {
       const int st = lt % stages;
       if (!mbar_wait(&full[st], (lt / stages) & 1)) {
         flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
@@ -213,58 +226,49 @@ __global__ void __launch_bounds__(416, 1)
       }
       const uint32_t kt = ring_u + st * kStageBytes, vt = kt + kTileBytes;
       const int tile_pos = (t0 + lt) * kTileN;
-      const int pbase = tile_pos + pg * NPW;
 
-      // S = Q K^T for 16 rows x NPW positions
+      // S = Q K^T for 16 rows x 64 positions: 8 independent accumulators
       float s[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a[4];
-        if (kQReg) {
-          a[0] = qa[kQReg ? ks : 0][0];
-          a[1] = qa[kQReg ? ks : 0][1];
-          a[2] = qa[kQReg ? ks : 0][2];
-          a[3] = qa[kQReg ? ks : 0][3];
-        } else {
-          ldsm_x4(qs_u + sw128_offset(qrow, 2 * ks + (lane >> 4), Mpad), a[0], a[1], a[2], a[3]);
-        }
 #pragma unroll
         for (int np = 0; np < NT / 2; ++np) {
-          const int prow = pg * NPW + np * 16 + (lane & 7) + ((lane >> 4) << 3);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kt + sw128_offset(prow, 2 * ks + ((lane >> 3) & 1), kTileN), b0, b1, b2, b3);
-          mma_16816(s[2 * np], a, b0, b1);
-          mma_16816(s[2 * np + 1], a, b2, b3);
+          ldsm_x4(kt + sw128_offset(np * 16 + krow, 2 * ks + kchk, kTileN), b0, b1, b2, b3);
+          mma_16816(s[2 * np], qa[ks], b0, b1);
+          mma_16816(s[2 * np + 1], qa[ks], b2, b3);
         }
       }
 
       // Collect-2-Query capture (prefix positions only)
-      if (cap_warp && pbase < L) {
+      if (cap_warp && tile_pos < L) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int col = nt * 8 + 2 * c;
-          cb[r * kCapCols + col] = s[nt][0] * p.scale;
-          cb[r * kCapCols + col + 1] = s[nt][1] * p.scale;
-          cb[(r + 8) * kCapCols + col] = s[nt][2] * p.scale;
-          cb[(r + 8) * kCapCols + col + 1] = s[nt][3] * p.scale;
+          *reinterpret_cast<float2*>(&cb[r * kCapStride + col]) =
+              make_float2(s[nt][0] * p.scale, s[nt][1] * p.scale);
+          *reinterpret_cast<float2*>(&cb[(r + 8) * kCapStride + col]) =
+              make_float2(s[nt][2] * p.scale, s[nt][3] * p.scale);
         }
         __syncwarp();
-        if (lane < NPW) {
-          const int pos = pbase + lane;
+        const int s1 = (R > 1) ? g : 0;
+#pragma unroll
+        for (int jj = 0; jj < kTileN / 32; ++jj) {
+          const int j = jj * 32 + lane;
+          const int pos = tile_pos + j;
           if (pos < L) {
-            const int s1 = (R > 1) ? g : 0;
             if (p.capture_mode == VG_CAPTURE_GROUP_SUM) {
-              float G = cb[lane] + cb[s1 * kCapCols + lane];
+              float G = cb[j] + cb[s1 * kCapStride + j];
               for (int qi = 1; qi < g; ++qi)
-                G = G + (cb[qi * kCapCols + lane] + cb[(s1 + qi) * kCapCols + lane]);
+                G = G + (cb[qi * kCapStride + j] + cb[(s1 + qi) * kCapStride + j]);
               p.capture[((size_t)b * p.num_kv_heads + h) * p.max_prefix + pos] = G;
             } else {
               for (int qi = 0; qi < g; ++qi) {
                 const size_t base = ((size_t)b * p.num_q_heads + h * g + qi) * 2;
-                p.capture[base * p.max_prefix + pos] = cb[qi * kCapCols + lane];
-                p.capture[(base + 1) * p.max_prefix + pos] = cb[(s1 + qi) * kCapCols + lane];
+                p.capture[base * p.max_prefix + pos] = cb[qi * kCapStride + j];
+                p.capture[(base + 1) * p.max_prefix + pos] = cb[(s1 + qi) * kCapStride + j];
               }
             }
           }
@@ -272,17 +276,30 @@ __global__ void __launch_bounds__(416, 1)
         __syncwarp();
       }
 
-      // online softmax (base 2)
+      // online softmax (base 2); only the last tiles need the causal mask
       float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (tile_pos + kTileN <= L + 1) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int pos = pbase + nt * 8 + 2 * c + e;
-          s[nt][e] = (pos <= lim0) ? s[nt][e] * p.scale_log2 : -INFINITY;
-          s[nt][2 + e] = (pos <= lim1) ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
-          mx0 = fmaxf(mx0, s[nt][e]);
-          mx1 = fmaxf(mx1, s[nt][2 + e]);
+          for (int e = 0; e < 2; ++e) {
+            s[nt][e] *= p.scale_log2;
+            s[nt][2 + e] *= p.scale_log2;
+            mx0 = fmaxf(mx0, s[nt][e]);
+            mx1 = fmaxf(mx1, s[nt][2 + e]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int pos = tile_pos + nt * 8 + 2 * c + e;
+            s[nt][e] = (pos <= lim0) ? s[nt][e] * p.scale_log2 : -INFINITY;
+            s[nt][2 + e] = (pos <= lim1) ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
+            mx0 = fmaxf(mx0, s[nt][e]);
+            mx1 = fmaxf(mx1, s[nt][2 + e]);
+          }
         }
       }
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -296,12 +313,14 @@ __global__ void __launch_bounds__(416, 1)
       mrun1 = mn1;
       l0 *= corr0;
       l1 *= corr1;
+      if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
 #pragma unroll
-      for (int dn = 0; dn < DN; ++dn) {
-        acc[dn][0] *= corr0;
-        acc[dn][1] *= corr0;
-        acc[dn][2] *= corr1;
-        acc[dn][3] *= corr1;
+        for (int dn = 0; dn < DN; ++dn) {
+          acc[dn][0] *= corr0;
+          acc[dn][1] *= corr0;
+          acc[dn][2] *= corr1;
+          acc[dn][3] *= corr1;
+        }
       }
       uint32_t pa[NT / 2][4];
 #pragma unroll
@@ -318,14 +337,11 @@ __global__ void __launch_bounds__(416, 1)
       const bool ragged = tile_pos + kTileN > n_b;
 #pragma unroll
       for (int kk = 0; kk < NT / 2; ++kk) {
-        const int p0 = pg * NPW + kk * 16;
-        const int mi = lane >> 3;
-        const int prow = p0 + (lane & 7) + ((mi & 1) << 3);
-        const int posA = tile_pos + p0 + 2 * c;
+        const int posA = tile_pos + kk * 16 + 2 * c;
 #pragma unroll
         for (int dp = 0; dp < DN / 2; ++dp) {
           uint32_t v0, v1, v2, v3;
-          ldsm_x4_t(vt + sw128_offset(prow, 2 * dp + (mi >> 1), kTileN), v0, v1, v2, v3);
+          ldsm_x4_t(vt + sw128_offset(kk * 16 + vrow, 2 * dp + vchk, kTileN), v0, v1, v2, v3);
           if (ragged) {
             v0 = mask_pair(v0, posA, n_b);
             v2 = mask_pair(v2, posA, n_b);
@@ -346,11 +362,11 @@ __global__ void __launch_bounds__(416, 1)
   }
   __syncthreads();  // ring idle: every issued load was consumed
 
-  // ---------------------------------------------- merge the PG slices
+  // ---------------------------------------------- merge the NG tile groups
   float* sO = reinterpret_cast<float*>(ring);          // [n_cons][16][HD]
   float* sML = sO + (size_t)n_cons * 16 * HD;          // [n_cons][16][2]
-  float* sW = sML + (size_t)n_cons * 16 * 2;           // [M][PG]
-  float* sRow = sW + (size_t)Mpad * PG;                // [M][2]
+  float* sW = sML + (size_t)n_cons * 16 * 2;           // [M][NG]
+  float* sRow = sW + (size_t)Mpad * NG;                // [M][2]
   if (warp < n_cons) {
     float* o = sO + (size_t)warp * 16 * HD;
     const int r = lane >> 2, c = lane & 3;
@@ -371,19 +387,19 @@ __global__ void __launch_bounds__(416, 1)
   for (int m = threadIdx.x; m < M; m += blockDim.x) {
     const int mt = m >> 4, rr = m & 15;
     float mx = -INFINITY;
-    for (int pg = 0; pg < PG; ++pg) mx = fmaxf(mx, sML[((mt * PG + pg) * 16 + rr) * 2]);
+    for (int gq = 0; gq < NG; ++gq) mx = fmaxf(mx, sML[((gq * MT + mt) * 16 + rr) * 2]);
     const float ref = safe_ref(mx);
     float lt = 0.f;
-    for (int pg = 0; pg < PG; ++pg) {
-      const float w = ex2(sML[((mt * PG + pg) * 16 + rr) * 2] - ref);
-      sW[m * PG + pg] = w;
-      lt += w * sML[((mt * PG + pg) * 16 + rr) * 2 + 1];
+    for (int gq = 0; gq < NG; ++gq) {
+      const float w = ex2(sML[((gq * MT + mt) * 16 + rr) * 2] - ref);
+      sW[m * NG + gq] = w;
+      lt += w * sML[((gq * MT + mt) * 16 + rr) * 2 + 1];
     }
     sRow[m * 2] = mx;
     sRow[m * 2 + 1] = lt;
     if (p.splits == 1) {
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      for (int pg = 0; pg < PG; ++pg) sW[m * PG + pg] *= inv;
+      for (int gq = 0; gq < NG; ++gq) sW[m * NG + gq] *= inv;
     }
   }
   __syncthreads();
@@ -394,9 +410,10 @@ __global__ void __launch_bounds__(416, 1)
       const int m = e / (HD / 2), d = (e - m * (HD / 2)) * 2;
       const int mt = m >> 4, rr = m & 15;
       float o0 = 0.f, o1 = 0.f;
-      for (int pg = 0; pg < PG; ++pg) {
-        const float w = sW[m * PG + pg];
-        const float2 v = *reinterpret_cast<const float2*>(&sO[((size_t)(mt * PG + pg) * 16 + rr) * HD + d]);
+      for (int gq = 0; gq < NG; ++gq) {
+        const float w = sW[m * NG + gq];
+        const float2 v =
+            *reinterpret_cast<const float2*>(&sO[((size_t)(gq * MT + mt) * 16 + rr) * HD + d]);
         o0 += w * v.x;
         o1 += w * v.y;
       }
@@ -409,16 +426,17 @@ __global__ void __launch_bounds__(416, 1)
     return;
   }
 
-  // split-K: publish the partial, the last CTA of (b, h) merges
+  // split-K: publish the partial; verify_merge_kernel combines the splits
   float* po = p.part_o + ((bh * p.splits + split) * M) * HD;
   float* pml = p.part_ml + (bh * p.splits + split) * M * 2;
   for (int e = threadIdx.x; e < M * (HD / 2); e += blockDim.x) {
     const int m = e / (HD / 2), d = (e - m * (HD / 2)) * 2;
     const int mt = m >> 4, rr = m & 15;
     float o0 = 0.f, o1 = 0.f;
-    for (int pg = 0; pg < PG; ++pg) {
-      const float w = sW[m * PG + pg];
-      const float2 v = *reinterpret_cast<const float2*>(&sO[((size_t)(mt * PG + pg) * 16 + rr) * HD + d]);
+    for (int gq = 0; gq < NG; ++gq) {
+      const float w = sW[m * NG + gq];
+      const float2 v =
+          *reinterpret_cast<const float2*>(&sO[((size_t)(gq * MT + mt) * 16 + rr) * HD + d]);
       o0 += w * v.x;
       o1 += w * v.y;
     }
@@ -428,54 +446,77 @@ __global__ void __launch_bounds__(416, 1)
     pml[m * 2] = sRow[m * 2];
     pml[m * 2 + 1] = sRow[m * 2 + 1];
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *s_flag = (atomicAdd(&p.tickets[bh], 1) == p.splits - 1);
-  __syncthreads();
-  if (!*s_flag) return;
-  __threadfence();
+}
 
-  float* sWs = reinterpret_cast<float*>(ring);  // [splits][M]
-  const float* mlb = p.part_ml + bh * p.splits * M * 2;
-  for (int m = threadIdx.x; m < M; m += blockDim.x) {
-    float mx = -INFINITY;
-    for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, __ldcg(&mlb[((size_t)s * M + m) * 2]));
-    const float ref = safe_ref(mx);
-    float lt = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-      const float w = ex2(__ldcg(&mlb[((size_t)s * M + m) * 2]) - ref);
-      sWs[s * M + m] = w;
-      lt += w * __ldcg(&mlb[((size_t)s * M + m) * 2 + 1]);
-    }
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
-    for (int s = 0; s < p.splits; ++s) sWs[s * M + m] *= inv;
-  }
+// Split-K merge: one CTA per (output row m, KV head, sequence).  Thread t < splits
+// reads split t's (m, l); each of the HD / 4 threads of a float4 column then
+// sums the splits' partial rows with the log-sum-exp weights.  Launched with
+// programmatic dependent launch: it waits for the verify grid (and its
+// memory) before reading the partials.
+template <int HD>
+__global__ void __launch_bounds__(128) verify_merge_kernel(const VerifyParams p) {
+  __shared__ float w_s[kMaxSplits];
+  __shared__ float red[32];
+  const int m = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int L = p.prefix_lens[b];
+  if (L < 1 || L > p.max_prefix ||
+      (L + p.n_rows + kPageSize - 1) / kPageSize > p.max_pages_per_seq)
+    return;  // the verify kernel skipped this sequence (and flagged it)
+  const int M = p.m_rows, S = p.splits;
+  const size_t bh = (size_t)b * p.num_kv_heads + h;
+  const float* mlb = p.part_ml + bh * S * M * 2;
+  // max over splits (block-wide)
+  float mv = -INFINITY;
+  for (int s = tid; s < S; s += blockDim.x) mv = fmaxf(mv, __ldcg(&mlb[((size_t)s * M + m) * 2]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+  if (lane == 0) red[warp] = mv;
   __syncthreads();
-  const float* pob = p.part_o + bh * p.splits * M * HD;
-  for (int e = threadIdx.x; e < M * (HD / 4); e += blockDim.x) {
-    const int m = e / (HD / 4), d = (e - m * (HD / 4)) * 4;
+  float mx = -INFINITY;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
+  const float ref = safe_ref(mx);
+  __syncthreads();
+  float lv = 0.f;
+  for (int s = tid; s < S; s += blockDim.x) {
+    const float w = ex2(__ldcg(&mlb[((size_t)s * M + m) * 2]) - ref);
+    w_s[s] = w;
+    lv += w * __ldcg(&mlb[((size_t)s * M + m) * 2 + 1]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lv += __shfl_xor_sync(0xffffffffu, lv, o);
+  if (lane == 0) red[warp] = lv;
+  __syncthreads();
+  float lt = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) lt += red[w];
+  const float inv = lt > 0.f ? 1.f / lt : 0.f;
+  // weighted sum of the partial rows; every split's load is independent
+  const float* pob = p.part_o + bh * S * M * HD;
+  for (int d4 = tid; d4 < HD / 4; d4 += blockDim.x) {
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < p.splits; ++s) {
-      const float w = sWs[s * M + m];
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(&pob[((size_t)s * M + m) * HD + d]));
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) {
+      const float w = w_s[s];
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(&pob[((size_t)s * M + m) * HD + d4 * 4]));
       o.x += w * v.x;
       o.y += w * v.y;
       o.z += w * v.z;
       o.w += w * v.w;
     }
     int i, qi;
-    row_of(m, g, R, i, qi);
-    __nv_bfloat16* dst = &p.out[((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD + d];
-    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(o.x, o.y);
-    *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(o.z, o.w);
+    row_of(m, p.group, p.n_rows, i, qi);
+    __nv_bfloat16* dst =
+        &p.out[((size_t)(b * p.n_rows + i) * p.num_q_heads + h * p.group + qi) * HD + d4 * 4];
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+    *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(o.z * inv, o.w * inv);
   }
-  if (threadIdx.x == 0) p.tickets[bh] = 0;
 }
 
 struct VerifyPlan {
-  int hd, m_rows, m_tiles, pg, splits, tiles_per_split, stages;
+  int hd, m_rows, m_tiles, groups, splits, tiles_per_split, stages;
   size_t smem_bytes;
-  size_t off_ml, off_tickets, ws_bytes;
+  size_t off_ml, ws_bytes;
 };
 
 bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, int head_dim,
@@ -486,7 +527,8 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   pl->hd = head_dim;
   pl->m_rows = g * n_rows;
   pl->m_tiles = ceil_div(pl->m_rows, 16);
-  pl->pg = pl->m_tiles <= 3 ? 4 : 2;
+  // tile groups working on alternating tiles; consumers + producer <= 8 warps
+  pl->groups = pl->m_tiles == 1 ? 3 : (pl->m_tiles <= 3 ? 2 : 1);
   const int tiles = ceil_div(max_prefix + n_rows, kTileN);
   int tps;
   if (num_splits > 0) {
@@ -494,7 +536,7 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   } else {
     const int pairs = batch * num_kv_heads;
     const int sms = device_sm_count();
-    const int splits = std::max(1, sms / pairs);
+    int splits = std::max(1, sms / pairs);
     tps = ceil_div(tiles, splits);
     if (batch > 1) tps = std::min(tps, 32);  // ragged lengths: small chunks balance SMs
     tps = std::max(tps, std::min(tiles, 4));
@@ -503,42 +545,57 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   pl->tiles_per_split = tps;
   pl->splits = ceil_div(tiles, tps);
   const int stage_bytes = 2 * kTileN * head_dim * 2;
-  const int n_cons = pl->m_tiles * pl->pg;
+  const int n_cons = pl->m_tiles * pl->groups;
   const int mpad = pl->m_tiles * 16;
-  // the ring is reused after the main loop for the slice merge and the split merge
+  auto smem_for = [&](int stages) {
+    return 1024 + (size_t)stages * stage_bytes + (size_t)mpad * head_dim * 2 +
+           (size_t)pl->groups * 16 * 72 * 4 + 2 * stages * 8 + 16;
+  };
+  // ring depth: a multiple of the group count (see the consumer loop), 192 KB
+  // at head_dim 128, shrunk if the whole layout would not fit
+  int stages = (head_dim == 128 ? 6 : 12);
+  while (stages > pl->groups && smem_for(stages) > 227 * 1024) stages -= pl->groups;
+  // the ring is reused after the main loop for the merge of the tile groups
   const size_t merge_bytes =
-      std::max((size_t)n_cons * 16 * (head_dim + 2) * 4 + (size_t)mpad * (pl->pg + 2) * 4,
-               (size_t)pl->splits * pl->m_rows * 4);
-  pl->stages = std::max(4, (int)ceil_div((int)merge_bytes, stage_bytes));
-  pl->smem_bytes = 1024 + (size_t)pl->stages * stage_bytes + (size_t)mpad * head_dim * 2 +
-                   (size_t)pl->pg * 16 * 32 * 4 + 2 * pl->stages * 8 + 16;
+      (size_t)n_cons * 16 * (head_dim + 2) * 4 + (size_t)mpad * (pl->groups + 2) * 4;
+  if ((size_t)stages * stage_bytes < merge_bytes) return false;
+  pl->stages = stages;
+  pl->smem_bytes = smem_for(stages);
   const size_t o_bytes = (size_t)batch * num_kv_heads * pl->splits * pl->m_rows * head_dim * 4;
   const size_t ml_bytes = (size_t)batch * num_kv_heads * pl->splits * pl->m_rows * 2 * 4;
   pl->off_ml = align_up(o_bytes, 256);
-  pl->off_tickets = pl->off_ml + align_up(ml_bytes, 256);
-  pl->ws_bytes = pl->splits > 1 ? pl->off_tickets + align_up((size_t)batch * num_kv_heads * 4, 256)
-                                 : 0;
+  pl->ws_bytes = pl->splits > 1 ? pl->off_ml + align_up(ml_bytes, 256) : 0;
   return true;
 }
 
-template <int HD, int PG>
+template <int HD>
 cudaError_t launch_verify(const VerifyPlan& pl, const CUtensorMap& tk, const CUtensorMap& tv,
                           const VerifyParams& p, dim3 grid, cudaStream_t stream) {
   static bool attr_set[64] = {false};
-  static size_t attr_bytes[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && (!attr_set[dev] || attr_bytes[dev] < pl.smem_bytes)) {
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<HD, PG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)std::max<size_t>(pl.smem_bytes, 200 * 1024));
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
-    attr_bytes[dev] = std::max<size_t>(pl.smem_bytes, 200 * 1024);
   }
-  const int threads = (pl.m_tiles * PG + 1) * 32;
-  verify_kernel<HD, PG><<<grid, threads, pl.smem_bytes, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  const int threads = (pl.m_tiles * pl.groups + 1) * 32;
+  verify_kernel<HD><<<grid, threads, pl.smem_bytes, stream>>>(tk, tv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || pl.splits == 1) return e;
+  // split merge, chained with programmatic dependent launch
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.m_rows, p.num_kv_heads, p.batch);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_merge_kernel<HD>, p);
 }
 
 }  // namespace
@@ -597,7 +654,6 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.part_o = pl.ws_bytes ? reinterpret_cast<float*>(ws) : nullptr;
   p.part_ml = pl.ws_bytes ? reinterpret_cast<float*>(ws + pl.off_ml) : nullptr;
-  p.tickets = pl.ws_bytes ? reinterpret_cast<int32_t*>(ws + pl.off_tickets) : nullptr;
   p.error_flag = error_flag;
   p.batch = batch;
   p.n_rows = n_rows;
@@ -613,23 +669,19 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
   p.splits = pl.splits;
   p.tiles_per_split = pl.tiles_per_split;
   p.stages = pl.stages;
+  p.groups = pl.groups;
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * kLog2e;
   dim3 grid(pl.splits, kv->num_kv_heads, batch);
-  cudaError_t e;
-  if (kv->head_dim == 128)
-    e = pl.pg == 4 ? launch_verify<128, 4>(pl, tk, tv, p, grid, stream)
-                   : launch_verify<128, 2>(pl, tk, tv, p, grid, stream);
-  else
-    e = pl.pg == 4 ? launch_verify<64, 4>(pl, tk, tv, p, grid, stream)
-                   : launch_verify<64, 2>(pl, tk, tv, p, grid, stream);
+  const cudaError_t e = kv->head_dim == 128 ? launch_verify<128>(pl, tk, tv, p, grid, stream)
+                                             : launch_verify<64>(pl, tk, tv, p, grid, stream);
   return e == cudaSuccess ? VG_OK : VG_ERR_LAUNCH;
 }
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of vg_verify_attention (declared in vg.h).
 //
-// Its split partials and merge tickets live in one file-scope device array of
+// Its split partials live in one file-scope device array of
 // fixed size instead of a caller-provided workspace.  The array exists once
 // per GPU that loads this library and stays resident until the process exits.
 namespace {
@@ -677,13 +729,8 @@ extern "C" vg_status vg_verify_attention_noalloc(const vg_paged_kv* kv, const vo
   if (pl.ws_bytes > kNoAllocScratchBytes) return VG_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* scratch = static_cast<uint8_t*>(noalloc_scratch_on_current_device());
   if (!scratch) return VG_ERR_LAUNCH;
-  if (pl.ws_bytes > 0) {
-    // The array keeps the previous call's contents: the merge tickets must
-    // start at zero, the partials are always written before they are read.
-    if (cudaMemsetAsync(scratch + pl.off_tickets, 0, (size_t)batch * kv->num_kv_heads * 4,
-                        stream) != cudaSuccess)
-      return VG_ERR_LAUNCH;
-  }
+  // The array keeps the previous call's contents; nothing in it has to start
+  // at zero: every partial is written before the merge reads it.
   return vg_verify_attention(kv, q, prefix_lens, batch, n_rows, num_q_heads, max_prefix,
                              softmax_scale, out, capture_mode, capture, num_splits, scratch,
                              kNoAllocScratchBytes, error_flag, stream);

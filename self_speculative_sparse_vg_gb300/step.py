@@ -3,6 +3,7 @@
 every computation happens in libvg's kernels."""
 from __future__ import annotations
 
+import ctypes
 from dataclasses import dataclass, field
 from typing import Optional
 
@@ -70,25 +71,47 @@ class DecodeStep:
     def max_tail(self):
         return max(self.spec.n_drafts, 1)
 
+    # The C calls are made with argument tuples built once per stream (the
+    # buffers never move), so a launch costs one ctypes call.
+    def _args(self, kind, t, stream):
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        key = (kind, t, s.cuda_stream)
+        cache = self.extra.setdefault("args", {})
+        if key in cache:
+            return cache[key]
+        p = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+        sp, st = self.spec, ctypes.c_void_p(s.cuda_stream)
+        kvs = self.extra.setdefault("kv_struct", self.kv.struct())
+        B, R, Hq, d = self.q_verify.shape
+        if kind == "verify":
+            a = (ctypes.byref(kvs), p(self.q_verify), p(self.prefix_lens), B, R, Hq,
+                 sp.max_prefix, ctypes.c_float(sp.softmax_scale), p(self.out_verify),
+                 self.capture_mode, p(self.capture), self.num_splits, p(self.ws_verify),
+                 self.ws_verify.numel(), p(self.error_flag), st)
+        elif kind == "select":
+            a = (p(self.capture), self.capture_mode, p(self.prefix_lens), B, Hq, sp.num_kv_heads,
+                 sp.max_prefix, sp.top_k, sp.n_sink, sp.n_recent, int(self.per_head),
+                 p(self.indices), p(self.counts), self.indices.shape[-1], None, 0,
+                 p(self.error_flag), st)
+        else:
+            a = (ctypes.byref(kvs), p(self.draft_q[t - 1]), p(self.indices), p(self.counts),
+                 int(self.per_head), self.indices.shape[-1], p(self.tail_start),
+                 p(self.cur_len[t - 1]), B, Hq, self.max_tail, ctypes.c_float(sp.softmax_scale),
+                 p(self.out_draft[t - 1]), p(self.ws_draft), self.ws_draft.numel(),
+                 p(self.error_flag), st)
+        cache[key] = a
+        return a
+
     def verify(self, stream=None):
-        s = self.spec
-        vg.verify_attention(self.kv, self.q_verify, self.prefix_lens, s.max_prefix, s.softmax_scale,
-                            self.out_verify, self.capture_mode, self.capture, self.num_splits,
-                            self.ws_verify, self.error_flag, stream)
+        vg._check("vg_verify_attention", vg._lib.vg_verify_attention(*self._args("verify", 0, stream)))
 
     def select(self, stream=None):
-        s = self.spec
-        vg.select_kv(self.capture, self.capture_mode, self.prefix_lens, s.num_q_heads,
-                     s.num_kv_heads, s.max_prefix, s.top_k, s.n_sink, s.n_recent, self.per_head,
-                     self.indices, self.counts, self.error_flag, stream)
+        vg._check("vg_select_kv", vg._lib.vg_select_kv(*self._args("select", 0, stream)))
 
     def draft(self, t: int, stream=None):
         """Draft step t = 1..k: query at position L + t - 1, tail [L, L + t)."""
-        s = self.spec
-        vg.sparse_draft_attention(self.kv, self.draft_q[t - 1], self.indices, self.counts,
-                                  self.per_head, self.tail_start, self.cur_len[t - 1],
-                                  self.max_tail, s.softmax_scale, self.out_draft[t - 1],
-                                  self.ws_draft, self.error_flag, stream)
+        vg._check("vg_sparse_draft_attention",
+                  vg._lib.vg_sparse_draft_attention(*self._args("draft", t, stream)))
 
     def run(self, stream=None):
         self.verify(stream)
@@ -97,4 +120,6 @@ class DecodeStep:
             self.draft(t, stream)
 
     def launches_per_step(self) -> int:
-        return 2 + self.spec.n_drafts
+        """Kernels of one step: verify (+ its split merge), select, k drafts."""
+        merge = 1 if self.ws_verify.numel() > 1 else 0
+        return 2 + merge + self.spec.n_drafts

@@ -56,6 +56,7 @@ def _kv(head_dim=128, page_size=16, k=0x1000, v=0x2000, table=0x3000):
 def test_host_argument_checks_without_gpu():
     """Every call below is rejected by host validation before any CUDA call."""
     from self_speculative_sparse_vg_gb300 import vg
+    from self_speculative_sparse_vg_gb300.vg import PagedKVStruct
     L = vg._lib
     fake = ctypes.c_void_p(0x4000)
     # null KV struct / null pointers
@@ -85,10 +86,12 @@ def test_host_argument_checks_without_gpu():
     # cache too small for max_prefix + rows (64 pages * 16 = 1024 positions)
     assert L.vg_verify_attention(ctypes.byref(kv), fake, fake, 1, 6, 32, 1020, 0.1, fake, 1, fake,
                                  0, None, 0, None, None) == 1
-    # missing workspace when the plan needs split partials (forced 4 splits)
-    assert L.vg_verify_workspace_bytes(1, 6, 32, 8, 128, 1000, 4) > 0
-    assert L.vg_verify_attention(ctypes.byref(kv), fake, fake, 1, 6, 32, 1000, 0.1, fake, 1, fake,
-                                 4, None, 0, None, None) == 3
+    # missing workspace when the plan needs split partials (20 forced splits:
+    # more than one cluster holds, so they merge through the workspace)
+    kv2 = PagedKVStruct(0x1000, 0x2000, 0x3000, 400, 16, 400, 8, 128)
+    assert L.vg_verify_workspace_bytes(1, 6, 32, 8, 128, 5000, 24) > 0
+    assert L.vg_verify_attention(ctypes.byref(kv2), fake, fake, 1, 6, 32, 5000, 0.1, fake, 1, fake,
+                                 24, None, 0, None, None) == 3
     # select: cap too small, bad mode, non-divisible heads
     assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 50, None, 0,
                           None, None) == 1
@@ -98,9 +101,11 @@ def test_host_argument_checks_without_gpu():
                           None, None) == 1
     assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 300000, 100, 4, 16, 0, fake, fake, 200, None, 0,
                           None, None) == 2
-    # sparse draft: g > 8, missing workspace
+    # sparse draft: g > 8; a list longer than 16 CTAs x 8 chunks x 64 entries
     assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 200, fake, fake, 1,
                                        80, 5, 0.1, fake, None, 0, None, None) == 2
-    assert L.vg_sparse_draft_workspace_bytes(1, 32, 8, 128, 200, 5) > 0
-    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 200, fake, fake, 1,
-                                       32, 5, 0.1, fake, None, 0, None, None) == 3
+    assert L.vg_sparse_draft_workspace_bytes(1, 32, 8, 128, 200, 5) == 0
+    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 9000, fake, fake, 1,
+                                       32, 5, 0.1, fake, None, 0, None, None) == 2
+    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, None, fake, 0, 200, fake, fake, 1,
+                                       32, 5, 0.1, fake, None, 0, None, None) == 1

@@ -23,7 +23,7 @@ def _require_gpu():
         pytest.skip("no GPU")
 
 
-@pytest.mark.parametrize("num_splits", [5, 0, 1])
+@pytest.mark.parametrize("num_splits", [24, 5, 0, 1])  # 24: split scratch in use
 def test_noalloc_verify_matches_workspace_entry_point(num_splits):
     _require_gpu()
     from self_speculative_sparse_vg_gb300 import vg
@@ -45,6 +45,8 @@ def test_noalloc_verify_matches_workspace_entry_point(num_splits):
     vg.verify_attention(kv, q, lens, Lmax, spec.softmax_scale, ref_out, vg.CAPTURE_GROUP_SUM,
                         ref_cap, num_splits, ws, flag)
 
+    if num_splits == 24:
+        assert vg.verify_workspace_bytes(B, R, Hq, Hkv, d, Lmax, num_splits) > 0
     st = kv.struct()
     for _ in range(2):  # two calls in a row share the library's scratch
         out = torch.full((B, R, Hq, d), float("nan"), dtype=torch.bfloat16, device=dev)
