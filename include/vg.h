@@ -176,10 +176,10 @@ vg_status vg_select_kv(const float* capture, int capture_mode, const int32_t* pr
  *               cur_len), 0 <= cur_len - tail_start <= max_tail.
  *   out         bf16 [batch][num_q_heads][head_dim].
  * The attended list (selection, then tail) is processed in chunks of 64
- * entries by one thread-block cluster per (sequence, KV head), merged in
- * distributed shared memory; no workspace is needed
- * (vg_sparse_draft_workspace_bytes returns 0; workspace may be NULL).
- * Supported: head_dim 64/128, g in [1, 8], cap + max_tail <= 8192.
+ * entries, one CTA each, which write fp32 partials to the workspace; a
+ * second, small kernel (programmatic dependent launch, same stream) merges
+ * them into `out`.
+ * Supported: head_dim 64/128, g in [1, 8], cap + max_tail <= 65536.
  * ------------------------------------------------------------------------- */
 size_t vg_sparse_draft_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
                                        int head_dim, int cap, int max_tail);

@@ -128,6 +128,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   __shared__ int wb[96];
   extern __shared__ __align__(16) uint32_t keys[];  // [slice]
 
+  // programmatic dependent launch: the capture comes from the previous kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int L = p.prefix_lens[b];
   int32_t* out = p.indices + ((size_t)b * p.rows + row) * p.cap;
   if (L < 0 || L > p.max_prefix) {  // same decision in every CTA of the cluster
@@ -356,13 +359,15 @@ extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
   cfg.blockDim = dim3(kSelThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)slice * 4;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel, p);
   return e == cudaSuccess ? VG_OK : VG_ERR_LAUNCH;
 }

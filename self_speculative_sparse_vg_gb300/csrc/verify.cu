@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(cbuf + NG * 16 * kCapStride);
   uint64_t* empty = full + stages;
 
+  // programmatic dependent launch: inputs may come from the previous kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int L = p.prefix_lens[b];
   const int n_b = L + R;
   if (L < 1 || L > p.max_prefix || (n_b + kPageSize - 1) / kPageSize > p.max_pages_per_seq) {
@@ -454,63 +457,22 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
 // programmatic dependent launch: it waits for the verify grid (and its
 // memory) before reading the partials.
 template <int HD>
-__global__ void __launch_bounds__(128) verify_merge_kernel(const VerifyParams p) {
-  __shared__ float w_s[kMaxSplits];
-  __shared__ float red[32];
+__global__ void __launch_bounds__(kMergeThreads) verify_merge_kernel(const VerifyParams p) {
+  __shared__ __align__(16) float smem_f[kMergeSmemFloats];
   const int m = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int L = p.prefix_lens[b];
   if (L < 1 || L > p.max_prefix ||
       (L + p.n_rows + kPageSize - 1) / kPageSize > p.max_pages_per_seq)
     return;  // the verify kernel skipped this sequence (and flagged it)
   const int M = p.m_rows, S = p.splits;
   const size_t bh = (size_t)b * p.num_kv_heads + h;
-  const float* mlb = p.part_ml + bh * S * M * 2;
-  // max over splits (block-wide)
-  float mv = -INFINITY;
-  for (int s = tid; s < S; s += blockDim.x) mv = fmaxf(mv, __ldcg(&mlb[((size_t)s * M + m) * 2]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
-  if (lane == 0) red[warp] = mv;
-  __syncthreads();
-  float mx = -INFINITY;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, red[w]);
-  const float ref = safe_ref(mx);
-  __syncthreads();
-  float lv = 0.f;
-  for (int s = tid; s < S; s += blockDim.x) {
-    const float w = ex2(__ldcg(&mlb[((size_t)s * M + m) * 2]) - ref);
-    w_s[s] = w;
-    lv += w * __ldcg(&mlb[((size_t)s * M + m) * 2 + 1]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lv += __shfl_xor_sync(0xffffffffu, lv, o);
-  if (lane == 0) red[warp] = lv;
-  __syncthreads();
-  float lt = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) lt += red[w];
-  const float inv = lt > 0.f ? 1.f / lt : 0.f;
-  // weighted sum of the partial rows; every split's load is independent
-  const float* pob = p.part_o + bh * S * M * HD;
-  for (int d4 = tid; d4 < HD / 4; d4 += blockDim.x) {
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int s = 0; s < S; ++s) {
-      const float w = w_s[s];
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(&pob[((size_t)s * M + m) * HD + d4 * 4]));
-      o.x += w * v.x;
-      o.y += w * v.y;
-      o.z += w * v.z;
-      o.w += w * v.w;
-    }
-    int i, qi;
-    row_of(m, p.group, p.n_rows, i, qi);
-    __nv_bfloat16* dst =
-        &p.out[((size_t)(b * p.n_rows + i) * p.num_q_heads + h * p.group + qi) * HD + d4 * 4];
-    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(o.x * inv, o.y * inv);
-    *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(o.z * inv, o.w * inv);
-  }
+  int i, qi;
+  row_of(m, p.group, p.n_rows, i, qi);
+  merge_splits<HD>(p.part_o + (bh * S * M + m) * HD, (size_t)M * HD, p.part_ml + (bh * S * M + m) * 2,
+                   (size_t)M * 2, S,
+                   p.out + ((size_t)(b * p.n_rows + i) * p.num_q_heads + h * p.group + qi) * HD, smem_f);
 }
 
 struct VerifyPlan {
@@ -580,14 +542,22 @@ cudaError_t launch_verify(const VerifyPlan& pl, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int threads = (pl.m_tiles * pl.groups + 1) * 32;
-  verify_kernel<HD><<<grid, threads, pl.smem_bytes, stream>>>(tk, tv, p);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t vcfg = {};
+  vcfg.gridDim = grid;
+  vcfg.blockDim = dim3((pl.m_tiles * pl.groups + 1) * 32, 1, 1);
+  vcfg.dynamicSmemBytes = pl.smem_bytes;
+  vcfg.stream = stream;
+  vcfg.attrs = pdl;
+  vcfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&vcfg, verify_kernel<HD>, tk, tv, p);
   if (e != cudaSuccess || pl.splits == 1) return e;
   // split merge, chained with programmatic dependent launch
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.m_rows, p.num_kv_heads, p.batch);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.blockDim = dim3(kMergeThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -185,4 +185,104 @@ __device__ __forceinline__ float ex2(float x) {
 // exp2 with a -inf-safe reference: when the running max is still -inf, use 0
 __device__ __forceinline__ float safe_ref(float m) { return m == -INFINITY ? 0.f : m; }
 
+// ------------------------------------------------------------ split merge
+// Log-sum-exp merge of S partial rows, run by one CTA of kMergeThreads:
+//   out[d] = sum_s 2^(m_s - M) O_s[d] / sum_s 2^(m_s - M) l_s,  M = max_s m_s,
+// with O_s the unnormalised partial (relative to its own m_s, base 2).
+// o_base[s * o_stride + d] and ml_base[s * ml_stride + {0, 1}] = (m_s, l_s);
+// the merged row goes to dst[0 .. HD) as bf16.
+// Thread t owns float4 column t % (HD / 4) for splits t / (HD / 4) + k * G;
+// every split's loads are issued before any is used (one round trip for
+// S <= G * kMergePer), then the G split groups are reduced in shared memory.
+constexpr int kMergeThreads = 256;
+constexpr int kMergePer = 8;
+
+constexpr int kMergeSmemFloats = 8 + 128 + 4 * kMergeThreads;
+
+template <int HD>
+__device__ __forceinline__ void merge_splits(const float* o_base, size_t o_stride,
+                                             const float* ml_base, size_t ml_stride, int S,
+                                             __nv_bfloat16* dst, float* smem_f) {
+  constexpr int COLS = HD / 4;
+  constexpr int G = kMergeThreads / COLS;
+  const int t = threadIdx.x, col = t % COLS, grp = t / COLS;
+  float* red = smem_f;                                         // [8]
+  float* w_s = smem_f + 8;                                     // [G * kMergePer] of a batch
+  float4* part = reinterpret_cast<float4*>(smem_f + 8 + 128);  // [G][COLS]
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float mx_all = -INFINITY, lt_all = 0.f;
+  for (int s0 = 0; s0 < S; s0 += G * kMergePer) {
+    float4 v[kMergePer];
+#pragma unroll
+    for (int k = 0; k < kMergePer; ++k) {
+      const int s = s0 + grp + k * G;
+      v[k] = s < S ? __ldcg(reinterpret_cast<const float4*>(o_base + (size_t)s * o_stride) + col)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // (m, l) of this batch's splits: thread t < batch size loads one pair
+    const int nb = min(S - s0, G * kMergePer);
+    float m_t = -INFINITY, l_t = 0.f;
+    if (t < nb) {
+      m_t = __ldcg(ml_base + (size_t)(s0 + t) * ml_stride);
+      l_t = __ldcg(ml_base + (size_t)(s0 + t) * ml_stride + 1);
+    }
+    float mw = m_t;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+    __syncthreads();
+    if ((t & 31) == 0) red[t >> 5] = mw;
+    __syncthreads();
+    float mb = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) mb = fmaxf(mb, red[w]);
+    const float m_new = fmaxf(mx_all, mb);
+    const float ref = safe_ref(m_new);
+    const float corr = ex2(mx_all - ref);
+    if (t < nb) w_s[t] = ex2(m_t - ref);
+    float lw = t < nb ? ex2(m_t - ref) * l_t : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+    __syncthreads();
+    if ((t & 31) == 0) red[t >> 5] = lw;
+    __syncthreads();
+    float lb = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) lb += red[w];
+    lt_all = lt_all * corr + lb;
+    mx_all = m_new;
+    acc.x *= corr;
+    acc.y *= corr;
+    acc.z *= corr;
+    acc.w *= corr;
+#pragma unroll
+    for (int k = 0; k < kMergePer; ++k) {
+      const int s = s0 + grp + k * G;
+      if (s < S) {
+        const float w = w_s[grp + k * G];
+        acc.x += w * v[k].x;
+        acc.y += w * v[k].y;
+        acc.z += w * v[k].z;
+        acc.w += w * v[k].w;
+      }
+    }
+  }
+  part[grp * COLS + col] = acc;
+  __syncthreads();
+  if (grp == 0) {
+    float4 o = part[col];
+#pragma unroll
+    for (int k = 1; k < G; ++k) {
+      const float4 q = part[k * COLS + col];
+      o.x += q.x;
+      o.y += q.y;
+      o.z += q.z;
+      o.w += q.w;
+    }
+    const float inv = lt_all > 0.f ? 1.f / lt_all : 0.f;
+    *reinterpret_cast<__nv_bfloat162*>(dst + col * 4) = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+    *reinterpret_cast<__nv_bfloat162*>(dst + col * 4 + 2) =
+        __floats2bfloat162_rn(o.z * inv, o.w * inv);
+  }
+}
+
 }  // namespace vg

@@ -120,6 +120,7 @@ class DecodeStep:
             self.draft(t, stream)
 
     def launches_per_step(self) -> int:
-        """Kernels of one step: verify (+ its split merge), select, k drafts."""
+        """Kernels of one step: verify (+ its split merge), select, k drafts
+        (each a chunk kernel plus its merge)."""
         merge = 1 if self.ws_verify.numel() > 1 else 0
-        return 2 + merge + self.spec.n_drafts
+        return 2 + merge + 2 * self.spec.n_drafts

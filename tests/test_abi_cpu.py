@@ -101,11 +101,13 @@ def test_host_argument_checks_without_gpu():
                           None, None) == 1
     assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 300000, 100, 4, 16, 0, fake, fake, 200, None, 0,
                           None, None) == 2
-    # sparse draft: g > 8; a list longer than 16 CTAs x 8 chunks x 64 entries
+    # sparse draft: g > 8; a list longer than 1024 chunks of 64; missing workspace
     assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 200, fake, fake, 1,
                                        80, 5, 0.1, fake, None, 0, None, None) == 2
-    assert L.vg_sparse_draft_workspace_bytes(1, 32, 8, 128, 200, 5) == 0
-    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 9000, fake, fake, 1,
-                                       32, 5, 0.1, fake, None, 0, None, None) == 2
+    assert L.vg_sparse_draft_workspace_bytes(1, 32, 8, 128, 200, 5) > 0
+    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 70000, fake, fake, 1,
+                                       32, 5, 0.1, fake, fake, 1 << 30, None, None) == 2
+    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 200, fake, fake, 1,
+                                       32, 5, 0.1, fake, None, 0, None, None) == 3
     assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, None, fake, 0, 200, fake, fake, 1,
                                        32, 5, 0.1, fake, None, 0, None, None) == 1
