@@ -6,10 +6,12 @@
 // the Whole, "What carries the argument": sink and recent tokens are always
 // kept; per-head index variant.
 //
-// Design: one thread-block cluster of C CTAs per selection row.  CTA c owns a
-// contiguous slice of positions, forms the fp32 scores in the documented
-// order, maps them to order-preserving 32-bit keys held in shared memory, and
-// takes part in a 4-pass MSB-first 8-bit radix select whose 256-bin
+// Design: a score kernel, spread over many CTAs, forms every position's fp32
+// score in the documented order and stores its order-preserving 32-bit key in
+// the workspace.  Then one thread-block cluster of C (<= 16) CTAs per
+// selection row: CTA c loads the keys of a contiguous slice of positions into
+// shared memory and takes part in an MSB-first 8-bit radix select (at most 4
+// passes, fewer once the whole boundary bin is kept) whose 256-bin
 // histograms are summed across the cluster through distributed shared memory
 // (double-buffered, one cluster barrier per pass).  That yields the exact
 // top_k-th key T.  Keys > T are all kept; keys == T are kept by ascending
@@ -34,6 +36,7 @@ constexpr int kMaxSlice = 16384;  // keys per CTA (64 KB of shared memory)
 
 struct SelectParams {
   const float* capture;
+  uint32_t* keys_ws;  // [B][rows][max_prefix] order-preserving score keys
   const int32_t* prefix_lens;
   int32_t* indices;
   int32_t* counts;
@@ -114,6 +117,20 @@ __device__ __forceinline__ int block_excl_count(bool f, int* wb, int* total) {
   return r;
 }
 
+// Score pass, spread over many CTAs (one position per thread): the fixed-order
+// fp32 score of every prefix position, stored as its order-preserving key.
+constexpr int kScoreThreads = 256;
+
+__global__ void __launch_bounds__(kScoreThreads) select_score_kernel(const SelectParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int row = blockIdx.y, b = blockIdx.z;
+  const int L = p.prefix_lens[b];
+  const int j = blockIdx.x * kScoreThreads + threadIdx.x;
+  if (L < 0 || L > p.max_prefix || L <= p.n_sink + p.n_recent + p.top_k || j >= L) return;
+  p.keys_ws[((size_t)b * p.rows + row) * p.max_prefix + j] = score_key(row_score(p, b, row, j));
+}
+
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectParams p) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
@@ -124,7 +141,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   __shared__ uint32_t hist[2][256];
   __shared__ uint32_t tot_s[256];
   __shared__ int cnt[2];    // this CTA's candidate keys > T and == T
-  __shared__ int ctl[4];    // digit, remaining k, gt_before, eq_before
+  __shared__ int ctl[5];    // digit, remaining k, gt_before, eq_before, boundary-bin count
   __shared__ int wb[96];
   extern __shared__ __align__(16) uint32_t keys[];  // [slice]
 
@@ -151,8 +168,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   }
   const int c_lo = p.n_sink, c_hi = L - p.n_recent;  // candidates [c_lo, c_hi)
 
+  const uint32_t* kw = p.keys_ws + ((size_t)b * p.rows + row) * p.max_prefix + lo;
 #pragma unroll 4
-  for (int j = tid; j < n_loc; j += blockDim.x) keys[j] = score_key(row_score(p, b, row, lo + j));
+  for (int j = tid; j < n_loc; j += blockDim.x) keys[j] = __ldcg(kw + j);
   __syncthreads();
 
   // ---- exact top_k-th largest candidate key: 4 passes of 8 bits, MSB first
@@ -203,6 +221,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
           if (above < (uint32_t)krem && above + t >= (uint32_t)krem) {
             ctl[0] = d;
             ctl[1] = krem - (int)above;
+            ctl[4] = (int)t;
           }
           above += t;
         }
@@ -211,10 +230,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
       prefix |= (uint32_t)ctl[0] << shift;
       mask |= 255u << shift;
       krem = ctl[1];
+      const bool whole_bin = (ctl[4] == krem);  // every key of the boundary bin is kept
       __syncthreads();
+      if (whole_bin) break;  // same decision in every CTA (same cluster-wide histogram)
     }
   }
-  const uint32_t T = prefix;  // exact key of the top_k-th candidate; krem of the == T keys are kept
+  // Keys are compared on the bits fixed so far (all 32 unless the search
+  // stopped early because the whole boundary bin is kept): (key & mask) > T
+  // is kept, and krem of the (key & mask) == T keys are kept, lowest
+  // positions first.
+  const uint32_t T = prefix;
 
   // ---- per-CTA counts of > T and == T, exclusive prefix over lower ranks
   if (tid < 2) cnt[tid] = 0;
@@ -224,7 +249,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
     for (int j = tid; j < n_loc; j += blockDim.x) {
       const int pos = lo + j;
       if (pos >= c_lo && pos < c_hi) {
-        const uint32_t k = keys[j];
+        const uint32_t k = keys[j] & mask;
         gt += k > T;
         eq += k == T;
       }
@@ -267,7 +292,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
       const int j = it * blockDim.x + tid;
       const int pos = lo + j;
       const bool in = j < n_loc && pos >= c_lo && pos < c_hi;
-      const uint32_t k = in ? keys[j] : 0u;
+      const uint32_t k = in ? (keys[j] & mask) : 0u;
       const bool is_gt = in && k > T, is_eq = in && k == T;
       int tot;
       const int eq_rank = eq_run + block_excl_count(is_eq, wb, &tot);
@@ -289,8 +314,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
 
 bool select_shape(int max_prefix, int* C, int* slice) {
   int c = 1;
-  while (c < 8 && ceil_div(max_prefix, c) > kTargetSlice) c *= 2;
-  while (c < kMaxCluster && ceil_div(max_prefix, c) > kMaxSlice) c *= 2;
+  while (c < kMaxCluster && ceil_div(max_prefix, c) > kTargetSlice) c *= 2;
   const int s = align_up(ceil_div(max_prefix, c), 4);
   if (s > kMaxSlice) return false;
   *C = c;
@@ -303,13 +327,18 @@ bool select_shape(int max_prefix, int* C, int* slice) {
 
 using namespace vg;
 
-extern "C" size_t vg_select_workspace_bytes(int, int, int, int) { return 0; }
+extern "C" size_t vg_select_workspace_bytes(int batch, int num_kv_heads, int max_prefix,
+                                            int per_head) {
+  if (batch <= 0 || num_kv_heads <= 0 || max_prefix <= 0) return 0;
+  const size_t rows = per_head ? num_kv_heads : 1;
+  return align_up((size_t)batch * rows * max_prefix * 4, 256);
+}
 
 extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
                                   const int32_t* prefix_lens, int batch, int num_q_heads,
                                   int num_kv_heads, int max_prefix, int top_k, int n_sink,
                                   int n_recent, int per_head, int32_t* indices, int32_t* counts,
-                                  int cap, void* /*workspace*/, size_t /*workspace_bytes*/,
+                                  int cap, void* workspace, size_t workspace_bytes,
                                   int32_t* error_flag, cudaStream_t stream) {
   if (!capture || !prefix_lens || !indices || !counts || batch <= 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || max_prefix <= 0 || top_k < 0 || n_sink < 0 || n_recent < 0 || cap <= 0)
@@ -322,9 +351,12 @@ extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
   if (cap < std::min<long long>(max_prefix, budget)) return VG_ERR_INVALID_ARGUMENT;
   int C, slice;
   if (!select_shape(max_prefix, &C, &slice)) return VG_ERR_UNSUPPORTED;
+  const size_t ws_need = vg_select_workspace_bytes(batch, num_kv_heads, max_prefix, per_head);
+  if (!workspace || workspace_bytes < ws_need) return VG_ERR_WORKSPACE_TOO_SMALL;
 
   SelectParams p;
   p.capture = capture;
+  p.keys_ws = static_cast<uint32_t*>(workspace);
   p.prefix_lens = prefix_lens;
   p.indices = indices;
   p.counts = counts;
@@ -354,6 +386,16 @@ extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
       return VG_ERR_LAUNCH;
     attr_done[dev] = true;
   }
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t scfg = {};
+  scfg.gridDim = dim3(ceil_div(max_prefix, kScoreThreads), p.rows, batch);
+  scfg.blockDim = dim3(kScoreThreads, 1, 1);
+  scfg.stream = stream;
+  scfg.attrs = pdl;
+  scfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&scfg, select_score_kernel, p) != cudaSuccess) return VG_ERR_LAUNCH;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, p.rows, batch);
   cfg.blockDim = dim3(kSelThreads, 1, 1);

@@ -490,7 +490,7 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   pl->m_rows = g * n_rows;
   pl->m_tiles = ceil_div(pl->m_rows, 16);
   // tile groups working on alternating tiles; consumers + producer <= 8 warps
-  pl->groups = pl->m_tiles == 1 ? 3 : (pl->m_tiles <= 3 ? 2 : 1);
+  pl->groups = pl->m_tiles <= 2 ? 3 : (pl->m_tiles <= 3 ? 2 : 1);
   const int tiles = ceil_div(max_prefix + n_rows, kTileN);
   int tps;
   if (num_splits > 0) {

@@ -32,6 +32,7 @@ class DecodeStep:
     cur_len: torch.Tensor           # [k][B]
     ws_verify: torch.Tensor
     ws_draft: torch.Tensor
+    ws_select: torch.Tensor
     error_flag: torch.Tensor
     num_splits: int = 0
     extra: dict = field(default_factory=dict)
@@ -56,6 +57,7 @@ class DecodeStep:
         cur = torch.stack([prefix + t for t in range(1, k + 1)]) if k else prefix[None][:0]
         wsv = vg.zero_workspace(vg.verify_workspace_bytes(B, R, Hq, Hkv, d, Lmax, num_splits), dev)
         wsd = vg.zero_workspace(vg.sparse_draft_workspace_bytes(B, Hq, Hkv, d, cap, max(k, 1)), dev)
+        wss = vg.zero_workspace(vg.select_workspace_bytes(B, Hkv, Lmax, per_head), dev)
         return cls(spec=s, device=dev, kv=kv, q_verify=inp.q_verify.to(dev),
                    draft_q=inp.draft_q.to(dev), prefix_lens=prefix, capture_mode=capture_mode,
                    per_head=per_head, capture=capture,
@@ -64,7 +66,7 @@ class DecodeStep:
                    counts=torch.zeros(B, rows, dtype=torch.int32, device=dev),
                    out_draft=torch.zeros(max(k, 1), B, Hq, d, dtype=torch.bfloat16, device=dev),
                    tail_start=prefix.clone(), cur_len=cur.contiguous(), ws_verify=wsv,
-                   ws_draft=wsd, error_flag=torch.zeros(1, dtype=torch.int32, device=dev),
+                   ws_draft=wsd, ws_select=wss, error_flag=torch.zeros(1, dtype=torch.int32, device=dev),
                    num_splits=num_splits)
 
     @property
@@ -91,8 +93,8 @@ class DecodeStep:
         elif kind == "select":
             a = (p(self.capture), self.capture_mode, p(self.prefix_lens), B, Hq, sp.num_kv_heads,
                  sp.max_prefix, sp.top_k, sp.n_sink, sp.n_recent, int(self.per_head),
-                 p(self.indices), p(self.counts), self.indices.shape[-1], None, 0,
-                 p(self.error_flag), st)
+                 p(self.indices), p(self.counts), self.indices.shape[-1], p(self.ws_select),
+                 self.ws_select.numel(), p(self.error_flag), st)
         else:
             a = (ctypes.byref(kvs), p(self.draft_q[t - 1]), p(self.indices), p(self.counts),
                  int(self.per_head), self.indices.shape[-1], p(self.tail_start),
@@ -120,7 +122,7 @@ class DecodeStep:
             self.draft(t, stream)
 
     def launches_per_step(self) -> int:
-        """Kernels of one step: verify (+ its split merge), select, k drafts
-        (each a chunk kernel plus its merge)."""
+        """Kernels of one step: verify (+ its split merge), select (score pass
+        and cluster select), k drafts (each a chunk kernel plus its merge)."""
         merge = 1 if self.ws_verify.numel() > 1 else 0
-        return 2 + merge + 2 * self.spec.n_drafts
+        return 3 + merge + 2 * self.spec.n_drafts  # select = score pass + cluster select

@@ -168,15 +168,25 @@ def verify_attention_noalloc(kv: PagedKV, q, prefix_lens, max_prefix, softmax_sc
 
 
 # --------------------------------------------------------------------- select
+def select_workspace_bytes(batch, num_kv_heads, max_prefix, per_head) -> int:
+    return int(_lib.vg_select_workspace_bytes(batch, num_kv_heads, max_prefix, int(bool(per_head))))
+
+
 def select_kv(capture, capture_mode, prefix_lens, num_q_heads, num_kv_heads, max_prefix, top_k,
-              n_sink, n_recent, per_head, indices, counts, error_flag=None, stream=None):
-    """vg_select_kv.  indices int32 [B][rows][cap], counts int32 [B][rows]."""
+              n_sink, n_recent, per_head, indices, counts, error_flag=None, stream=None,
+              workspace=None):
+    """vg_select_kv.  indices int32 [B][rows][cap], counts int32 [B][rows].
+    workspace: uint8 device tensor of select_workspace_bytes() (allocated here
+    when not given)."""
     B = prefix_lens.shape[0]
     cap = indices.shape[-1]
+    if workspace is None:
+        workspace = zero_workspace(select_workspace_bytes(B, num_kv_heads, max_prefix, per_head),
+                                   indices.device)
     s = _lib.vg_select_kv(_ptr(capture), int(capture_mode), _ptr(prefix_lens), B, num_q_heads,
                           num_kv_heads, int(max_prefix), int(top_k), int(n_sink), int(n_recent),
-                          int(bool(per_head)), _ptr(indices), _ptr(counts), cap, None, 0,
-                          _ptr(error_flag), _stream(stream))
+                          int(bool(per_head)), _ptr(indices), _ptr(counts), cap, _ptr(workspace),
+                          workspace.numel(), _ptr(error_flag), _stream(stream))
     _check("vg_select_kv", s)
     return indices, counts
 

@@ -101,6 +101,12 @@ def test_host_argument_checks_without_gpu():
                           None, None) == 1
     assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 300000, 100, 4, 16, 0, fake, fake, 200, None, 0,
                           None, None) == 2
+    # select: the score-key workspace is missing or too small
+    assert L.vg_select_workspace_bytes(1, 8, 5000, 0) >= 5000 * 4
+    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None, 0,
+                          None, None) == 3
+    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 1, fake, fake, 200, fake,
+                          5000 * 4, None, None) == 3
     # sparse draft: g > 8; a list longer than 1024 chunks of 64; missing workspace
     assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 200, fake, fake, 1,
                                        80, 5, 0.1, fake, None, 0, None, None) == 2
