@@ -206,3 +206,39 @@ def to_paged(k_dense, v_dense, shuffle=False, seed=0, extra_pages=0, max_pages=N
             pad[:, :n] = src
             dst[ids] = pad.view(Hkv, np_b, PAGE_SIZE, d).permute(1, 0, 2, 3)
     return table, kp, vp
+
+
+def make_capture(spec: WorkloadSpec, capture_mode: int, seed: int) -> torch.Tensor:
+    """Synthetic captured logits for exercising a selector on its own (the
+    same tensor is given to the kernel and to the checker).  Values are
+    N(0, 3) rounded to multiples of 1/8, so exact ties are frequent, with a
+    few large planted values.  capture_mode 1: [B][Hkv][Lmax];
+    2: [B][Hq][2][Lmax] (float32)."""
+    g = torch.Generator().manual_seed(seed)
+    B, Hq, Hkv, Lmax = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.max_prefix
+    shape = (B, Hkv, Lmax) if capture_mode == 1 else (B, Hq, 2, Lmax)
+    x = torch.round(torch.randn(shape, generator=g) * 3.0 * 8.0) / 8.0
+    flat = x.view(-1)
+    hot = torch.randint(0, flat.numel(), (max(1, flat.numel() // 500),), generator=g)
+    flat[hot] = 40.0
+    return x.float()
+
+
+def make_selection(spec: WorkloadSpec, per_head: bool, seed: int):
+    """Synthetic index lists for exercising the sparse draft kernel on its
+    own: per (sequence, row) a sorted set of min(L_b, budget) distinct prefix
+    positions drawn uniformly, padded with -1.  Returns (indices int32
+    [B][rows][cap], counts int32 [B][rows])."""
+    g = torch.Generator().manual_seed(seed)
+    B = spec.batch
+    rows = spec.num_kv_heads if per_head else 1
+    cap = min(spec.max_prefix, spec.n_sel_max)
+    idx = torch.full((B, rows, cap), -1, dtype=torch.int32)
+    cnt = torch.zeros(B, rows, dtype=torch.int32)
+    for b, L in enumerate(spec.prefix_lens):
+        n = min(L, spec.n_sel_max)
+        for r in range(rows):
+            pos = torch.randperm(L, generator=g)[:n].sort().values
+            idx[b, r, :n] = pos.to(torch.int32)
+            cnt[b, r] = n
+    return idx, cnt

@@ -88,17 +88,37 @@ def gpu_sets(st):
     return sets
 
 
-def check_select_mirror(st, inp):
-    """Bit-exact against the oracle's fp32 mirror on the GPU's own capture."""
+def check_select_synthetic(spec, capture_mode, per_head, seed=5, device="cuda"):
+    """GPU selector vs the oracle's fp32 mirror, both fed the same
+    generator-made capture (with many exact ties): bit-exact index sets."""
+    from self_speculative_sparse_vg_gb300 import vg
+    from self_speculative_sparse_vg_gb300.workloads import make_capture
+    cap_cpu = make_capture(spec, capture_mode, seed)
+    rows = spec.num_kv_heads if per_head else 1
+    capn = min(spec.max_prefix, spec.n_sel_max)
+    idx = torch.full((spec.batch, rows, capn), -7, dtype=torch.int32, device=device)
+    cnt = torch.zeros(spec.batch, rows, dtype=torch.int32, device=device)
+    lens = torch.tensor(spec.prefix_lens, dtype=torch.int32, device=device)
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+    vg.select_kv(cap_cpu.to(device), capture_mode, lens, spec.num_q_heads, spec.num_kv_heads,
+                 spec.max_prefix, spec.top_k, spec.n_sink, spec.n_recent, per_head, idx, cnt, flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    ref = O.select_kv(cap_cpu.numpy(), capture_mode, spec.prefix_lens, spec.num_q_heads,
+                      spec.num_kv_heads, spec.top_k, spec.n_sink, spec.n_recent, per_head,
+                      mirror=True)
+    got_i, got_c = idx.cpu().numpy(), cnt.cpu().numpy()
+    for b in range(spec.batch):
+        for r in range(rows):
+            n = got_c[b, r]
+            assert got_i[b, r, :n].tolist() == ref[b][r].tolist(), f"select b={b} row={r}"
+            assert (got_i[b, r, n:] == -1).all(), "padding must be -1"
+
+
+def oracle_sets(inp, rows64, per_head):
     s = inp.spec
-    cap = st.capture.cpu().numpy()
-    ref = O.select_kv(cap, st.capture_mode, s.prefix_lens, s.num_q_heads, s.num_kv_heads, s.top_k,
-                      s.n_sink, s.n_recent, st.per_head, mirror=True)
-    got = gpu_sets(st)
-    for b in range(s.batch):
-        for r in range(len(ref[b])):
-            assert got[b][r].tolist() == ref[b][r].tolist(), f"select b={b} row={r}"
-    return ref
+    return O.select_kv(rows64, O.CAPTURE_ROWS, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
+                       s.top_k, s.n_sink, s.n_recent, per_head)
 
 
 def check_select_end_to_end(st, inp, rows64):
@@ -124,20 +144,55 @@ def check_select_end_to_end(st, inp, rows64):
     return worst
 
 
-def check_drafts(st, inp, sets, pairs=None, steps=None):
+def check_drafts(st, inp, oracle_sel, pairs=None, steps=None):
+    """GPU drafts (run on the GPU's own selection) vs the oracle's drafts on
+    the oracle's selection, for the (sequence, KV head) pairs whose two
+    selections are identical.  Returns the number of pairs compared."""
     s = inp.spec
     _, k, v = dense64(inp)
     g = s.group
     steps = steps or list(range(1, s.n_drafts + 1))
     pairs = pairs or [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
+    mine = gpu_sets(st)
+    same = [(b, h) for b, h in pairs
+            if mine[b][h if st.per_head else 0].tolist() == oracle_sel[b][h if st.per_head else 0].tolist()]
+    for t in steps:
+        dq = inp.draft_q[t - 1].double().numpy()
+        got = st.out_draft[t - 1].float().cpu().numpy()
+        for b, h in same:
+            sel = [[oracle_sel[b][h if st.per_head else 0]]]
+            ref = O.sparse_draft_attention(dq[b:b + 1, h * g:(h + 1) * g], [k[b][h:h + 1]],
+                                           [v[b][h:h + 1]], sel, False, [s.prefix_lens[b]],
+                                           [s.prefix_lens[b] + t], s.softmax_scale)
+            assert_close_out(got[b, h * g:(h + 1) * g], ref[0], f"draft t={t} b={b} h={h}")
+    return len(same)
+
+
+def check_drafts_synthetic(st, inp, per_head, seed=9, pairs=None, steps=None):
+    """GPU sparse draft vs the oracle, both fed the same generator-made index
+    lists (the GPU selection in `st` is overwritten)."""
+    from self_speculative_sparse_vg_gb300.workloads import make_selection
+    s = inp.spec
+    idx, cnt = make_selection(s, per_head, seed)
+    st.indices.copy_(idx.to(st.indices.device))
+    st.counts.copy_(cnt.to(st.counts.device))
+    steps = steps or list(range(1, s.n_drafts + 1))
+    for t in steps:
+        st.draft(t)
+    torch.cuda.synchronize()
+    assert int(st.error_flag.item()) == 0
+    _, k, v = dense64(inp)
+    g = s.group
+    pairs = pairs or [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
+    sel = [[idx[b, r, :cnt[b, r]].numpy() for r in range(idx.shape[1])] for b in range(s.batch)]
     for t in steps:
         dq = inp.draft_q[t - 1].double().numpy()
         got = st.out_draft[t - 1].float().cpu().numpy()
         for b, h in pairs:
-            sel = [[sets[b][h if st.per_head else 0]]]
             ref = O.sparse_draft_attention(dq[b:b + 1, h * g:(h + 1) * g], [k[b][h:h + 1]],
-                                           [v[b][h:h + 1]], sel, False, [s.prefix_lens[b]],
-                                           [s.prefix_lens[b] + t], s.softmax_scale)
+                                           [v[b][h:h + 1]], [[sel[b][h if per_head else 0]]], False,
+                                           [s.prefix_lens[b]], [s.prefix_lens[b] + t],
+                                           s.softmax_scale)
             assert_close_out(got[b, h * g:(h + 1) * g], ref[0], f"draft t={t} b={b} h={h}")
 
 
