@@ -242,3 +242,111 @@ def make_selection(spec: WorkloadSpec, per_head: bool, seed: int):
             idx[b, r, :n] = pos.to(torch.int32)
             cnt[b, r] = n
     return idx, cnt
+
+
+# ------------------------------------------------------------------ layer stack
+@dataclass(frozen=True)
+class StackSpec:
+    """A decoder attention stack driven through several draft/verify
+    iterations.  The Llama-3-8B-shaped default is 32 layers of hidden 4096,
+    32 query / 8 KV heads of 128, batch 4 at contexts 32K/64K/96K/128K, k = 5
+    drafts, a 2048 + 4 + 64 selection budget, 200 iterations and Bernoulli(0.7)
+    acceptance of each draft."""
+    name: str = "llama8b_stack32_b4"
+    layers: int = 32
+    hidden: int = 4096
+    num_q_heads: int = 32
+    num_kv_heads: int = 8
+    head_dim: int = 128
+    prefix_lens: tuple = (32768, 65536, 98304, 131072)
+    n_drafts: int = 5
+    top_k: int = 2048
+    n_sink: int = 4
+    n_recent: int = 64
+    iterations: int = 200
+    accept_p: float = 0.7
+    per_head: bool = False
+    seed: int = 6
+
+    @property
+    def batch(self) -> int:
+        return len(self.prefix_lens)
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def room(self) -> int:
+        """Cache positions written past L_b over a run: the first token, then
+        at most k + 1 committed per iteration, plus one block of k + 1 beyond."""
+        return 1 + (self.iterations + 1) * (self.n_drafts + 1)
+
+    @property
+    def max_prefix(self) -> int:
+        return max(self.prefix_lens) + self.room
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def n_sel_max(self) -> int:
+        return self.n_sink + self.n_recent + self.top_k
+
+
+STACKS = {"llama8b_stack32_b4": StackSpec()}
+
+
+def small_stack(**kw) -> StackSpec:
+    """A stack the float64 oracle runs in seconds: two layers, two sequences
+    of a few thousand positions, a few iterations, the Llama-3-8B head shape."""
+    base = StackSpec(name="small_stack", layers=2, prefix_lens=(1203, 2170), n_drafts=5,
+                     top_k=96, n_sink=4, n_recent=32, iterations=4, seed=21)
+    return replace(base, **kw)
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    return torch.Generator(device=torch.device(device)).manual_seed(seed)
+
+
+def make_stack_weights(spec: StackSpec, layer: int, device="cpu"):
+    """Q, K, V projection weights of one layer: bf16 [hidden][heads * d],
+    entries N(0, 1/hidden) (random initialisation; no checkpoint is read)."""
+    s = spec
+    g = _gen(device, s.seed * 7919 + 2 * layer)
+    std = 1.0 / math.sqrt(s.hidden)
+    out = []
+    for n in (s.num_q_heads, s.num_kv_heads, s.num_kv_heads):
+        w = torch.randn(s.hidden, n * s.head_dim, generator=g, device=device) * std
+        out.append(w.to(torch.bfloat16))
+    return tuple(out)
+
+
+def make_stack_context(spec: StackSpec, layer: int, device="cpu"):
+    """The initial context of one layer: per sequence b, bf16 K and V
+    [Hkv][L_b][d] with entries N(0, 1)."""
+    s = spec
+    g = _gen(device, s.seed * 7919 + 2 * layer + 1)
+    ks, vs = [], []
+    for L in s.prefix_lens:
+        ks.append(torch.randn(s.num_kv_heads, L, s.head_dim, generator=g, device=device)
+                  .to(torch.bfloat16))
+        vs.append(torch.randn(s.num_kv_heads, L, s.head_dim, generator=g, device=device)
+                  .to(torch.bfloat16))
+    return ks, vs
+
+
+def make_stack_embedding(spec: StackSpec, device="cpu") -> torch.Tensor:
+    """Input vector of the first decoded token of each sequence: float64
+    [B][hidden], entries N(0, 1)."""
+    g = _gen(device, spec.seed * 7919 - 1)
+    return torch.randn(spec.batch, spec.hidden, generator=g, device=device, dtype=torch.float64)
+
+
+def make_acceptance(spec: StackSpec) -> torch.Tensor:
+    """Per iteration, sequence and draft a Bernoulli(accept_p) draw: bool
+    [iterations][B][k].  These stand in for the accept/reject decisions of
+    speculative sampling, which need a trained model."""
+    g = torch.Generator().manual_seed(spec.seed * 7919 - 2)
+    return torch.rand(spec.iterations, spec.batch, spec.n_drafts, generator=g) < spec.accept_p

@@ -10,3 +10,11 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def ensure_lib():
+    """Build libvg.so in-tree if it is not there (nvcc cross-compiles without a GPU)."""
+    lib = os.path.join(ROOT, "self_speculative_sparse_vg_gb300", "libvg.so")
+    if not os.path.exists(lib):
+        from self_speculative_sparse_vg_gb300 import build
+        build.build()
