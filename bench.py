@@ -61,6 +61,23 @@ def algorithmic_bytes(spec, capture_mode=1):
             "step": verify + select + drafts, "verify_kv": verify_kv}
 
 
+def rank_env():
+    """(rank, world size, local rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def reduce_max(values, world, device=None):
+    """Each value's maximum over the ranks (the slowest rank sets the job's
+    time); a no-op for one rank.  Every rank gets the result."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -221,9 +238,7 @@ def main():
     args = ap.parse_args()
     assert args.warmup >= 3
 
-    rank = int(os.environ.get("RANK", 0))
-    world = int(os.environ.get("WORLD_SIZE", 1))
-    local = int(os.environ.get("LOCAL_RANK", 0))
+    rank, world, local = rank_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
@@ -355,10 +370,7 @@ def main():
         sum(m[2 * j].elapsed_time(m[2 * j + 1]) for j in range(k + 1)) * 1e3 for m in e2e_marks)
     assert torch.equal(ix_h, st.indices.cpu())
 
-    vals = torch.tensor([local_val, e2e_us, hot_us], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    value, e2e_val, hot_val = (float(x) for x in vals.cpu())
+    value, e2e_val, hot_val = reduce_max([local_val, e2e_us, hot_us], world, dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
