@@ -78,6 +78,27 @@ def reduce_max(values, world, device=None):
     return [float(x) for x in t.cpu()]
 
 
+def speedup_projection(alpha, k, t_draft, t_verify, t_select, t_dense):
+    """Projected speedup of self-speculative decoding over dense decoding,
+    attention only, from measured per-call times (µs).
+
+    A Sparse Glimpse of the Whole, "What carries the argument": speedup
+    S = (alpha k + 1) / (k gamma + 1), gamma = cost of a draft step relative
+    to a verification.  Here gamma = t_draft / (t_verify + t_select).  With
+    the accepted prefix rule (a draft counts only if every earlier one was
+    accepted) the tokens per iteration are E[a + 1] = (1 - alpha^(k+1)) /
+    (1 - alpha) instead of alpha k + 1; that variant is also given, with the
+    iteration cost measured against one dense one-row decode step t_dense."""
+    gamma = t_draft / (t_verify + t_select)
+    s_pages = (alpha * k + 1) / (k * gamma + 1)
+    tokens = (1 - alpha ** (k + 1)) / (1 - alpha) if alpha != 1 else k + 1
+    iteration = k * t_draft + t_verify + t_select
+    return {"alpha": alpha, "k": k, "gamma": gamma, "S_formula": s_pages,
+            "tokens_per_iteration_prefix_rule": tokens,
+            "S_measured_prefix_rule": tokens * t_dense / iteration,
+            "t_dense_decode_us": t_dense}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -370,6 +391,59 @@ def main():
         sum(m[2 * j].elapsed_time(m[2 * j + 1]) for j in range(k + 1)) * 1e3 for m in e2e_marks)
     assert torch.equal(ix_h, st.indices.cpu())
 
+    # ---------------- capture rules (Figure 6 analogue) and dense decode
+    # Verify alone under each capture mode, cold L2 each time; the Collect-2
+    # vs Collect-All selections are compared on the same inputs.  A one-row
+    # verify without capture is the dense decode step of the projection.
+    def time_verify(rows, mode, capture, ws, reps=30):
+        q = st.q_verify[:, :rows].contiguous()
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+        ts = []
+        for i in range(reps + 3):
+            flush(i)
+            a, b_ = ev(), ev()
+            a.record(stream)
+            vg.verify_attention(st.kv, q, st.prefix_lens, spec.max_prefix, spec.softmax_scale,
+                                out, mode, capture, 0, ws, st.error_flag)
+            b_.record(stream)
+            if i >= 3:
+                ts.append((a, b_))
+        torch.cuda.synchronize()
+        return statistics.median(x.elapsed_time(y) * 1e3 for x, y in ts)
+
+    B_, R_ = spec.batch, spec.n_rows
+    cap_rows = torch.zeros(B_, spec.num_q_heads, 2, spec.max_prefix, device=dev)
+    cap_all = torch.zeros_like(st.capture)
+    ws1 = vg.zero_workspace(vg.verify_workspace_bytes(B_, 1, spec.num_q_heads, spec.num_kv_heads,
+                                                      spec.head_dim, spec.max_prefix), dev)
+    capture_study = {
+        "verify_us_no_capture": time_verify(R_, vg.CAPTURE_NONE, None, st.ws_verify),
+        "verify_us_collect2_group_sum": time_verify(R_, vg.CAPTURE_GROUP_SUM, st.capture,
+                                                    st.ws_verify),
+        "verify_us_collect2_rows": time_verify(R_, vg.CAPTURE_ROWS, cap_rows, st.ws_verify),
+        "verify_us_collect_all": time_verify(R_, vg.CAPTURE_ALL_SUM, cap_all, st.ws_verify),
+    }
+    t_dense = time_verify(1, vg.CAPTURE_NONE, None, ws1)
+    idx2, cnt2 = st.indices.clone(), st.counts.clone()
+    vg.select_kv(st.capture, vg.CAPTURE_GROUP_SUM, st.prefix_lens, spec.num_q_heads,
+                 spec.num_kv_heads, spec.max_prefix, spec.top_k, spec.n_sink, spec.n_recent,
+                 st.per_head, idx2, cnt2, st.error_flag, workspace=st.ws_select)
+    idxa, cnta = st.indices.clone(), st.counts.clone()
+    vg.select_kv(cap_all, vg.CAPTURE_ALL_SUM, st.prefix_lens, spec.num_q_heads,
+                 spec.num_kv_heads, spec.max_prefix, spec.top_k, spec.n_sink, spec.n_recent,
+                 st.per_head, idxa, cnta, st.error_flag, workspace=st.ws_select)
+    torch.cuda.synchronize()
+    inter = tot = 0
+    for b_ in range(B_):
+        for r_ in range(idx2.shape[1]):
+            s2 = set(idx2[b_, r_, :int(cnt2[b_, r_])].tolist())
+            sa = set(idxa[b_, r_, :int(cnta[b_, r_])].tolist())
+            inter += len(s2 & sa)
+            tot += len(s2)
+    capture_study["selection_overlap_collect2_vs_all"] = inter / max(tot, 1)
+    del cap_rows, cap_all, ws1
+    assert int(st.error_flag.item()) == 0, "device error flag set"
+
     value, e2e_val, hot_val = reduce_max([local_val, e2e_us, hot_us], world, dev)
     if rank != 0:
         if world > 1:
@@ -400,6 +474,9 @@ def main():
         "e2e": {"value": e2e_val, "unit": "us", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * st.launches_per_step(),
+        "capture_rules": capture_study,
+        "projection": speedup_projection(0.7, k, statistics.mean(dra) / max(k, 1), v_mean,
+                                         statistics.mean(sel), t_dense),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:

@@ -64,7 +64,17 @@ enum {
   /* float32 [batch][num_q_heads][2][max_prefix]: slot 0 = row 0 (first draft
    * token), slot 1 = row k (bonus token).  With n_rows == 1 both slots hold
    * row 0.                                                                  */
-  VG_CAPTURE_ROWS = 2
+  VG_CAPTURE_ROWS = 2,
+  /* Collect-All-Query (Vegas, Figure 6 and "Core claim": the costlier rule
+   * that aggregates every verify row).  float32 [batch][num_kv_heads]
+   * [max_prefix], same layout as VG_CAPTURE_GROUP_SUM:
+   *   A[b][h][j] = sum over all n_rows rows and all query heads of KV head h
+   *                of s[q][i][j].
+   * Order: the g * n_rows (head, row) pairs are packed as [row 0 of each
+   * head][row k of each head][rows 1..k-1, head-major within a row]; each
+   * block of 16 consecutive pairs is reduced by a fixed butterfly, and the
+   * blocks' sums are added in ascending block order.                       */
+  VG_CAPTURE_ALL_SUM = 3
 };
 
 /* Bits OR-ed into *error_flag by the kernels. */
@@ -140,8 +150,9 @@ vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q, const int32_
  *   per_head == 0:  sum over KV heads h ascending of G[b][h][j]  (float32,
  *                   acc = G[0]; acc = acc + G[1]; ...),
  *   per_head != 0:  G[b][h][j],
- * where G is the capture itself (VG_CAPTURE_GROUP_SUM) or is formed from
- * VG_CAPTURE_ROWS in the order documented above.  The result is
+ * where G is the capture itself (VG_CAPTURE_GROUP_SUM, or VG_CAPTURE_ALL_SUM,
+ * which has the same layout) or is formed from VG_CAPTURE_ROWS in the order
+ * documented above.  The result is
  *   [0, n_sink) u [L_b - n_recent, L_b) u (the top_k positions of
  *   [n_sink, L_b - n_recent) by score descending, lower position first on
  *   equal scores),

@@ -39,6 +39,7 @@ import numpy as np
 
 CAPTURE_GROUP_SUM = 1   # per-KV-head sum of the two captured rows
 CAPTURE_ROWS = 2        # the two raw rows per query head
+CAPTURE_ALL_SUM = 3     # per-KV-head sum of every verify row (Collect-All)
 
 
 def _softmax_weights(s: np.ndarray) -> np.ndarray:
@@ -100,6 +101,28 @@ def capture_rows(q, k, prefix_lens, scale):
     return rows
 
 
+def collect_all_sum(q, k, prefix_lens, scale, num_kv_heads):
+    """Collect-All-Query capture: A[b,h,j] = sum over every verify row i and
+    every query head of KV head h of scale*q_{b,i,head}.k_j, for prefix
+    positions j < L_b (NaN beyond), float64.  [Vegas] Figure 6 and "Core
+    claim": the rule that aggregates all rows of the block, which Collect-2
+    replaces by its two boundary rows."""
+    B, R, Hq, d = q.shape
+    g = Hq // num_kv_heads
+    Lmax = int(max(prefix_lens))
+    A = np.full((B, num_kv_heads, Lmax), np.nan)
+    for b in range(B):
+        L = int(prefix_lens[b])
+        for h in range(num_kv_heads):
+            kp = k[b][h, :L]
+            acc = np.zeros(L)
+            for qh in range(h * g, (h + 1) * g):
+                for i in range(R):
+                    acc += scale * (kp @ q[b, i, qh])
+            A[b, h, :L] = acc
+    return A
+
+
 def group_sum(rows, num_kv_heads):
     """G[b,h,j] = sum over the query heads q of KV head h of
     (row0[q,j] + rowk[q,j]), float64.  [Vegas] "What carries the argument":
@@ -135,12 +158,12 @@ def selection_scores(capture, capture_mode, num_q_heads, num_kv_heads, per_head,
     [SSL] "What carries the argument": per-head variant, here one score per
     KV head (the unit at which GQA loads KV).
 
-    capture: GROUP_SUM -> [B][Hkv][Lmax];  ROWS -> [B][Hq][2][Lmax]
+    capture: GROUP_SUM or ALL_SUM -> [B][Hkv][Lmax];  ROWS -> [B][Hq][2][Lmax]
     returns  [B][1 or Hkv][Lmax]  (float64, or float32 when mirror)
     """
     if capture_mode == CAPTURE_ROWS:
         G = group_sum_mirror(capture, num_kv_heads) if mirror else group_sum(capture, num_kv_heads)
-    elif capture_mode == CAPTURE_GROUP_SUM:
+    elif capture_mode in (CAPTURE_GROUP_SUM, CAPTURE_ALL_SUM):
         G = np.asarray(capture, dtype=np.float32 if mirror else np.float64)
     else:
         raise ValueError("capture_mode")

@@ -343,6 +343,7 @@ extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
   if (!capture || !prefix_lens || !indices || !counts || batch <= 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || max_prefix <= 0 || top_k < 0 || n_sink < 0 || n_recent < 0 || cap <= 0)
     return VG_ERR_INVALID_ARGUMENT;
+  if (capture_mode == VG_CAPTURE_ALL_SUM) capture_mode = VG_CAPTURE_GROUP_SUM;  // same layout
   if (capture_mode != VG_CAPTURE_GROUP_SUM && capture_mode != VG_CAPTURE_ROWS)
     return VG_ERR_INVALID_ARGUMENT;
   if (num_q_heads % num_kv_heads) return VG_ERR_INVALID_ARGUMENT;

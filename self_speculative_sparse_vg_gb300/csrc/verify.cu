@@ -20,7 +20,11 @@
 //    reductions and rescales amortised over 64 positions).
 //  * Capture epilogue: the first-row-tile warps stage their 16 x 64 logits
 //    in shared memory and write either the raw two rows or their per-KV-head
-//    sum in a fixed order, with coalesced stores.
+//    sum in a fixed order, with coalesced stores.  Collect-All (every row)
+//    reduces each row tile's 16 rows per column with a butterfly, hands the
+//    partial column sums to the group's first warp through shared memory
+//    (mbarrier handshakes with bounded waits), which adds them in row-tile
+//    order and stores the per-KV-head sum.
 //  * Splits over the KV length write fp32 partials (O, m, l) to the
 //    workspace; a small merge kernel, one CTA per (output row, KV head,
 //    sequence), combines them.  It is chained with programmatic dependent
@@ -101,8 +105,11 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
   uint8_t* ring = smem;
   uint8_t* qs = ring + stages * kStageBytes;
   float* cbuf = reinterpret_cast<float*>(qs + Mpad * HD * 2);
-  uint64_t* full = reinterpret_cast<uint64_t*>(cbuf + NG * 16 * kCapStride);
+  float* cpart = cbuf + NG * 16 * kCapStride;  // Collect-All partials [NG][2][MT][64]
+  uint64_t* full = reinterpret_cast<uint64_t*>(cpart + NG * 2 * MT * kTileN);
   uint64_t* empty = full + stages;
+  uint64_t* capfull = empty + stages;  // [NG][2]: partials of a slot written
+  uint64_t* capfree = capfull + 2 * NG;  // [NG][2]: a slot read by the group's first warp
 
   // programmatic dependent launch: inputs may come from the previous kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -122,6 +129,10 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], MT);  // a tile is consumed by the MT warps of one group
+    }
+    for (int s = 0; s < 2 * NG; ++s) {
+      mbar_init(&capfull[s], MT > 1 ? MT - 1 : 1);
+      mbar_init(&capfree[s], 1);
     }
     fence_barrier_init();
   }
@@ -213,7 +224,10 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
     for (int ks = 0; ks < KS; ++ks)
       ldsm_x4(qs_u + sw128_offset(qrow, 2 * ks + (lane >> 4), Mpad), qa[ks][0], qa[ks][1],
               qa[ks][2], qa[ks][3]);
-    const bool cap_warp = (mt == 0) && (p.capture_mode != VG_CAPTURE_NONE);
+    const bool cap_warp =
+        (mt == 0) && (p.capture_mode == VG_CAPTURE_GROUP_SUM || p.capture_mode == VG_CAPTURE_ROWS);
+    const bool cap_all = p.capture_mode == VG_CAPTURE_ALL_SUM;
+    bool cap_live = true;  // false after a capture handshake timed out: wait no more
     float* cb = cbuf + grp * 16 * kCapStride;
     const uint32_t ring_u = smem_u32(ring);
     const int krow = (lane & 7) + ((lane >> 4) << 3);       // K ldmatrix row within 16
@@ -277,6 +291,61 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
           }
         }
         __syncwarp();
+      }
+
+      // Collect-All-Query capture: sum of every row of the tile's columns
+      if (cap_all && tile_pos < L) {
+        const int use_n = (lt - grp) / NG;  // this group's tile counter
+        const int slot = use_n & 1, use = use_n >> 1;
+        float* part = cpart + (size_t)(grp * 2 + slot) * MT * kTileN;
+        float cs[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            // rows r and r + 8 of this warp, then the 8 row pairs (lanes
+            // with the same c) by a fixed butterfly; padded rows hold zeros
+            float v = s[nt][e] * p.scale + s[nt][2 + e] * p.scale;
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            cs[nt][e] = v;
+          }
+        }
+        if (mt != 0 && use > 0 && cap_live &&
+            !mbar_wait(&capfree[grp * 2 + slot], (use - 1) & 1)) {
+          flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+          cap_live = false;
+        }
+        if (r == 0) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            *reinterpret_cast<float2*>(&part[mt * kTileN + nt * 8 + 2 * c]) =
+                make_float2(cs[nt][0], cs[nt][1]);
+        }
+        __syncwarp();
+        if (mt != 0) {
+          if (lane == 0) mbar_arrive(&capfull[grp * 2 + slot]);
+        } else {
+          if (MT > 1 && cap_live && !mbar_wait(&capfull[grp * 2 + slot], use & 1)) {
+            flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+            cap_live = false;
+          }
+          if (cap_live) {
+#pragma unroll
+            for (int jj = 0; jj < kTileN / 32; ++jj) {
+              const int j = jj * 32 + lane;
+              const int pos = tile_pos + j;
+              if (pos < L) {
+                float A = part[j];
+                for (int m2 = 1; m2 < MT; ++m2) A = A + part[m2 * kTileN + j];
+                p.capture[((size_t)b * p.num_kv_heads + h) * p.max_prefix + pos] = A;
+              }
+            }
+          }
+          __syncwarp();
+          if (MT > 1 && lane == 0) mbar_arrive(&capfree[grp * 2 + slot]);
+        }
       }
 
       // online softmax (base 2); only the last tiles need the causal mask
@@ -511,7 +580,8 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   const int mpad = pl->m_tiles * 16;
   auto smem_for = [&](int stages) {
     return 1024 + (size_t)stages * stage_bytes + (size_t)mpad * head_dim * 2 +
-           (size_t)pl->groups * 16 * 72 * 4 + 2 * stages * 8 + 16;
+           (size_t)pl->groups * 16 * 72 * 4 + (size_t)pl->groups * 2 * pl->m_tiles * kTileN * 4 +
+           2 * stages * 8 + 4 * pl->groups * 8 + 16;
   };
   // ring depth: a multiple of the group count (see the consumer loop), 192 KB
   // at head_dim 128, shrunk if the whole layout would not fit
@@ -595,7 +665,7 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
       max_prefix <= 0 || num_splits < 0 || !(softmax_scale == softmax_scale))
     return VG_ERR_INVALID_ARGUMENT;
   if (capture_mode != VG_CAPTURE_NONE && capture_mode != VG_CAPTURE_GROUP_SUM &&
-      capture_mode != VG_CAPTURE_ROWS)
+      capture_mode != VG_CAPTURE_ROWS && capture_mode != VG_CAPTURE_ALL_SUM)
     return VG_ERR_INVALID_ARGUMENT;
   if (capture_mode != VG_CAPTURE_NONE && !capture) return VG_ERR_INVALID_ARGUMENT;
   if (num_q_heads % kv->num_kv_heads) return VG_ERR_INVALID_ARGUMENT;

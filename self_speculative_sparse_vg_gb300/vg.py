@@ -18,6 +18,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvg.so")
 CAPTURE_NONE = 0
 CAPTURE_GROUP_SUM = 1
 CAPTURE_ROWS = 2
+CAPTURE_ALL_SUM = 3
 
 DEVERR_PAGE = 1
 DEVERR_INDEX = 2

@@ -65,10 +65,21 @@ def oracle_rows(inp):
     return O.capture_rows(q, k, inp.spec.prefix_lens, inp.spec.softmax_scale)
 
 
+def oracle_all(inp):
+    """Collect-All capture of the oracle, [B][Hkv][Lmax] float64."""
+    q, k, _ = dense64(inp)
+    s = inp.spec
+    return O.collect_all_sum(q, k, s.prefix_lens, s.softmax_scale, s.num_kv_heads)
+
+
 def check_capture(st, inp, rows64):
     s = inp.spec
     cap = st.capture.cpu().numpy()
-    if st.capture_mode == O.CAPTURE_ROWS:
+    if st.capture_mode == O.CAPTURE_ALL_SUM:
+        A = oracle_all(inp)
+        for b, L in enumerate(s.prefix_lens):
+            assert_close_capture(cap[b, :, :L], A[b, :, :L], f"collect-all b={b}")
+    elif st.capture_mode == O.CAPTURE_ROWS:
         for b, L in enumerate(s.prefix_lens):
             assert_close_capture(cap[b, :, :, :L], rows64[b, :, :, :L], f"rows b={b}")
     else:
@@ -115,17 +126,27 @@ def check_select_synthetic(spec, capture_mode, per_head, seed=5, device="cuda"):
             assert (got_i[b, r, n:] == -1).all(), "padding must be -1"
 
 
-def oracle_sets(inp, rows64, per_head):
+def _oracle_capture(inp, rows64, capture_mode):
+    """The oracle's capture for a capture mode: Collect-All sums, or the raw
+    rows (from which the Collect-2 group sums follow)."""
+    if capture_mode == O.CAPTURE_ALL_SUM:
+        return oracle_all(inp), O.CAPTURE_ALL_SUM
+    return rows64, O.CAPTURE_ROWS
+
+
+def oracle_sets(inp, rows64, per_head, capture_mode=O.CAPTURE_GROUP_SUM):
     s = inp.spec
-    return O.select_kv(rows64, O.CAPTURE_ROWS, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
+    cap, mode = _oracle_capture(inp, rows64, capture_mode)
+    return O.select_kv(cap, mode, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
                        s.top_k, s.n_sink, s.n_recent, per_head)
 
 
 def check_select_end_to_end(st, inp, rows64):
     """GPU capture -> GPU select vs float64 oracle capture -> float64 select."""
     s = inp.spec
-    sc = O.selection_scores(rows64, O.CAPTURE_ROWS, s.num_q_heads, s.num_kv_heads, st.per_head)
-    ref = O.select_kv(rows64, O.CAPTURE_ROWS, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
+    cap, mode = _oracle_capture(inp, rows64, st.capture_mode)
+    sc = O.selection_scores(cap, mode, s.num_q_heads, s.num_kv_heads, st.per_head)
+    ref = O.select_kv(cap, mode, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
                       s.top_k, s.n_sink, s.n_recent, st.per_head)
     got = gpu_sets(st)
     worst = 0.0

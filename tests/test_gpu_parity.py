@@ -59,6 +59,26 @@ def test_small_step(name, mode, per_head):
     P.check_drafts_synthetic(st, inp, per_head)
 
 
+COLLECT_ALL = ["base", "d64", "mha", "g8", "g5", "k0", "k1", "short", "m96"]
+SMALL_EXTRA = dict(m96=dict(num_q_heads=16, num_kv_heads=2, n_drafts=11))  # g*R = 96: 6 row tiles
+
+
+@pytest.mark.parametrize("name", COLLECT_ALL)
+@pytest.mark.parametrize("per_head", [False, True])
+def test_small_step_collect_all(name, per_head):
+    """Collect-All-Query capture (every verify row summed per KV head) and
+    selection on it, against the oracle."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    spec = small_spec(**{**SMALL, **SMALL_EXTRA}[name])
+    inp, st = _run(spec, capture_mode=3, per_head=per_head)
+    P.check_verify(st, inp)
+    rows64 = P.oracle_rows(inp)
+    P.check_capture(st, inp, rows64)
+    P.check_select_end_to_end(st, inp, rows64)
+    P.check_drafts(st, inp, P.oracle_sets(inp, rows64, per_head, capture_mode=3))
+
+
 def test_ties_select_lower_position():
     """All-equal captured scores: the kept candidates are the lowest positions."""
     _require_gpu()
@@ -172,7 +192,7 @@ def test_full_size_workload(name):
     _require_gpu()
     from self_speculative_sparse_vg_gb300.workloads import WORKLOADS
     spec = WORKLOADS[name]
-    modes = [(1, False), (2, True)] if spec.batch > 1 else [(1, False)]
+    modes = [(1, False), (2, True), (3, False)] if spec.batch > 1 else [(1, False), (3, True)]
     for mode, per_head in modes:
         inp, st = _run(spec, capture_mode=mode, per_head=per_head)
         if name == "tiny_d64_2k":
@@ -183,11 +203,12 @@ def test_full_size_workload(name):
         rows64 = P.oracle_rows(inp)
         P.check_capture(st, inp, rows64)
         P.check_select_end_to_end(st, inp, rows64)
-        osets = P.oracle_sets(inp, rows64, per_head)
+        osets = P.oracle_sets(inp, rows64, per_head, capture_mode=mode)
         P.check_drafts(st, inp, osets, pairs=pairs, steps=[1, spec.n_drafts])
         if name == "tiny_d64_2k":
             assert set(inp.planted[0].tolist()) <= set(P.gpu_sets(st)[0][0].tolist())
-        P.check_select_synthetic(spec, mode, per_head)
+        if mode != 3:  # Collect-All feeds the selector the same layout as mode 1
+            P.check_select_synthetic(spec, mode, per_head)
         P.check_drafts_synthetic(st, inp, per_head, pairs=pairs, steps=[1, spec.n_drafts])
         del st
         torch.cuda.empty_cache()

@@ -323,3 +323,38 @@ def test_capture_rows_equals_verify_capture():
     q, k, v = _rand_case(rng, 2, 4, 8, 2, 16, [19, 6])
     _, rows = O.verify_attention(q, k, v, [19, 6], 0.2)
     np.testing.assert_allclose(O.capture_rows(q, k, [19, 6], 0.2), rows, rtol=0, atol=1e-12)
+
+
+def test_collect_all_with_two_rows_equals_collect_two():
+    """With k = 1 the block has only rows 0 and k, so Collect-All and the
+    Collect-2 group sum are the same quantity."""
+    rng = np.random.default_rng(41)
+    q, k, _ = _rand_case(rng, 2, 2, 8, 2, 16, [23, 7])
+    A = O.collect_all_sum(q, k, [23, 7], 0.3, 2)
+    G = O.group_sum(O.capture_rows(q, k, [23, 7], 0.3), 2)
+    np.testing.assert_allclose(A, G, rtol=0, atol=1e-12)
+
+
+def test_collect_all_is_linear_in_the_rows():
+    """Summing logits over rows equals the logit of the summed query: a
+    one-row capture of sum_i q_i gives both Collect-2 slots equal to that
+    row, so Collect-All = half of its group sum."""
+    rng = np.random.default_rng(42)
+    q, k, _ = _rand_case(rng, 1, 6, 8, 2, 8, [40])
+    A = O.collect_all_sum(q, k, [40], 0.5, 2)
+    qs = q.sum(axis=1, keepdims=True)
+    G1 = O.group_sum(O.capture_rows(qs, k, [40], 0.5), 2)
+    np.testing.assert_allclose(A, G1 / 2, rtol=0, atol=1e-10)
+    # it differs from Collect-2 once the block has middle rows
+    G2 = O.group_sum(O.capture_rows(q, k, [40], 0.5), 2)
+    assert np.abs(A - G2).max() > 1e-3
+
+
+def test_collect_all_hand_values():
+    """d = 1, one KV head with keys [1, -2, 3], two query heads, three rows:
+    A_j = scale * k_j * (sum of all six query values)."""
+    q = np.array([[[[1.0], [2.0]], [[0.5], [-1.0]], [[4.0], [0.25]]]])   # [1][3][2][1]
+    k = [np.array([[[1.0], [-2.0], [3.0], [9.0], [9.0], [9.0]]])]        # [1][6][1]
+    A = O.collect_all_sum(q, k, [3], 2.0, 1)
+    total = 1 + 2 + 0.5 - 1 + 4 + 0.25
+    np.testing.assert_array_equal(A[0, 0], 2.0 * total * np.array([1.0, -2.0, 3.0]))
