@@ -188,7 +188,8 @@ vg_status vg_select_kv(const float* capture, int capture_mode, const int32_t* pr
  *   tail_start  int32 [batch]: the prefix length the selection was made on.
  *   cur_len     int32 [batch]: query position + 1; tail = [tail_start,
  *               cur_len), 0 <= cur_len - tail_start <= max_tail.
- *   out         bf16 [batch][num_q_heads][head_dim].
+ *   out         bf16 [batch][num_q_heads][head_dim]; zero when nothing is
+ *               attended (count 0 and an empty tail).
  * The attended list (selection, then tail) is processed in chunks of 64
  * entries, one CTA each, which write fp32 partials to the workspace; a
  * second, small kernel (programmatic dependent launch, same stream) merges

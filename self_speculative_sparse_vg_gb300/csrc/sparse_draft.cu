@@ -10,12 +10,13 @@
 // Design: one CTA per 64-entry chunk of the attended list (the selection,
 // then the tail [tail_start, cur_len)), per (KV head, sequence); all chunks of
 // a step are resident at once.
-//  * The chunk's selected positions, the sequence's page-table row (staged in
-//    shared memory when short), the query rows and the lengths are loaded
-//    together, so a row's address costs one round trip.
-//  * The chunk's K and V rows are gathered with 16-byte cp.async straight
-//    into the 128-byte-swizzled tile layout the verify kernel's TMA loads
-//    produce.
+//  * The chunk's selected positions, the sequence's page-table row (one bulk
+//    copy into shared memory when short), the query rows and the lengths are
+//    loaded together, so a row's address costs one round trip.
+//  * Each of the chunk's K and V rows (256 bytes at head_dim 128) is then one
+//    bulk copy (cp.async.bulk, completion counted on an mbarrier with a
+//    bounded wait) into a row-padded tile (row stride head_dim * 2 + 16
+//    bytes, so ldmatrix rows fall in distinct bank groups).
 //  * The g query heads of the KV head are the rows of a 16-row bf16
 //    mma.sync tile (zero padded); warp w takes positions [16w, 16w + 16),
 //    and P is reused as the A operand of P.V.
@@ -54,9 +55,13 @@ struct DraftParams {
 
 template <int HD>
 struct DraftLayout {
-  static constexpr int kTileBytes = kChunk * HD * 2;  // one of K / V
-  static constexpr int kQBytes = 16 * HD * 2;
-  static constexpr size_t kBytes = 1024 + 2 * (size_t)kTileBytes + kQBytes + (size_t)kPtMax * 4;
+  static constexpr int kRowBytes = HD * 2 + 16;             // padded K / V / Q row
+  static constexpr int kTileBytes = kChunk * kRowBytes;     // one of K / V
+  static constexpr int kQBytes = 16 * kRowBytes;
+  static constexpr int kOStride = 2 * 32 + 8;               // floats per (warp, n-tile) stash
+  static constexpr size_t kBytes = 1024 + 2 * (size_t)kTileBytes + kQBytes + (size_t)kPtMax * 4 + 64;
+  static_assert((size_t)kDraftWarps * (HD / 8) * kOStride * 4 <= 2 * (size_t)kTileBytes,
+                "the O stash reuses the K/V tiles");
 };
 
 // Sequence-level checks shared by both kernels; false if the sequence is skipped.
@@ -93,17 +98,26 @@ __global__ void __launch_bounds__(kDraftThreads)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* kt = smem;  // [64][HD] swizzled
+  constexpr int RB = Lay::kRowBytes;
+  uint8_t* kt = smem;  // [64][RB]
   uint8_t* vt = kt + Lay::kTileBytes;
-  uint8_t* qs = vt + Lay::kTileBytes;  // [16][HD] swizzled
+  uint8_t* qs = vt + Lay::kTileBytes;  // [16][RB]
   int32_t* pt_s = reinterpret_cast<int32_t*>(qs + Lay::kQBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pt_s + kPtMax);  // [0] page table, [1] K/V rows
   __shared__ long long off_s[kChunk];
   __shared__ float wm_s[kDraftWarps][16], wl_s[kDraftWarps][16];
 
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], kChunk);  // one arrival per row thread
+    fence_barrier_init();
+  }
+  __syncthreads();
+
   // One round trip for everything the addresses depend on: this chunk's
   // selected positions (read speculatively; the index array holds cap
-  // entries), the page-table row (staged when it is short), the query rows
-  // and the lengths.
+  // entries), the page-table row (one bulk copy when it is short), the
+  // query rows and the lengths.
   const int e = chunk * kChunk + tid;
   int pos_sel = -1;
   if (tid < kChunk && e < p.cap) pos_sel = __ldg(p.indices + ((size_t)b * rows + row) * p.cap + e);
@@ -111,24 +125,31 @@ __global__ void __launch_bounds__(kDraftThreads)
   if (pt_in_smem) {
     const int32_t* src = p.page_table + (size_t)b * p.max_pages_per_seq;
     const int n = p.max_pages_per_seq;
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-      for (int i = tid; i < n / 4; i += kDraftThreads) cp_async_16(pt_s + 4 * i, src + 4 * i);
-      for (int k = (n / 4) * 4 + tid; k < n; k += kDraftThreads) pt_s[k] = __ldg(src + k);
-    } else {
-      for (int k = tid; k < n; k += kDraftThreads) pt_s[k] = __ldg(src + k);
+    const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+    const int nb = aligned ? (n / 4) * 4 : 0;  // entries in the bulk copy (whole 16 bytes)
+    if (tid == 0) {
+      if (nb > 0) {
+        mbar_arrive_expect_tx(&bars[0], nb * 4);
+        bulk_load(pt_s, src, nb * 4, &bars[0]);
+      } else {
+        mbar_arrive(&bars[0]);
+      }
     }
+    for (int k = nb + tid; k < n; k += kDraftThreads) pt_s[k] = __ldg(src + k);
+  } else if (tid == 0) {
+    mbar_arrive(&bars[0]);
   }
-  cp_async_commit();
-  for (int idx = tid; idx < 16 * CH; idx += kDraftThreads) {  // query rows, swizzled, >= g zero
+  for (int idx = tid; idx < 16 * CH; idx += kDraftThreads) {  // query rows; rows >= g zero
     const int r = idx / CH, ch = idx - (idx / CH) * CH;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < g)
       v = *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.num_q_heads + h * g + r) * HD + ch * 8);
-    *reinterpret_cast<uint4*>(qs + sw128_offset(r, ch, 16)) = v;
+    *reinterpret_cast<uint4*>(qs + r * RB + ch * 16) = v;
   }
   int cnt, ts, cl;
   const bool lengths_ok = draft_lengths(p, b, row, rows, &cnt, &ts, &cl);
-  cp_async_wait<0>();  // no copy may still be landing when the CTA leaves
+  // the page-table copy must land before anything reads it or the CTA leaves
+  if (!mbar_wait(&bars[0], 0)) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
   if (!lengths_ok) {
     if (tid == 0 && chunk == 0)
       flag_error(p.error_flag, cnt < 0 || cnt > p.cap ? VG_DEVERR_COUNT : VG_DEVERR_LENGTH);
@@ -139,7 +160,8 @@ __global__ void __launch_bounds__(kDraftThreads)
   if (ne <= 0) return;  // past the end of this list: no partial
   __syncthreads();
 
-  // resolve: element offset of each entry's K/V row, -1 if none (zero row, masked)
+  // resolve each entry's K/V row and issue its two bulk copies; rows without
+  // an entry (past the list, bad index or page) are zero and masked below
   if (tid < kChunk) {
     long long off = -1;
     if (tid < ne) {
@@ -164,34 +186,33 @@ __global__ void __launch_bounds__(kDraftThreads)
       }
     }
     off_s[tid] = off;
-  }
-  __syncthreads();
-  // gather K and V rows into the swizzled tiles
-  for (int idx = tid; idx < kChunk * CH; idx += kDraftThreads) {
-    const int j = idx / CH, c = idx - (idx / CH) * CH;
-    const long long off = off_s[j];
-    const uint32_t o = sw128_offset(j, c, kChunk);
+    uint8_t* kd = kt + tid * RB;
+    uint8_t* vd = vt + tid * RB;
     if (off >= 0) {
-      cp_async_16(kt + o, p.k_pages + off + c * 8);
-      cp_async_16(vt + o, p.v_pages + off + c * 8);
+      mbar_arrive_expect_tx(&bars[1], 2 * HD * 2);
+      bulk_load(kd, p.k_pages + off, HD * 2, &bars[1]);
+      bulk_load(vd, p.v_pages + off, HD * 2, &bars[1]);
     } else {
-      *reinterpret_cast<uint4*>(kt + o) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(vt + o) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        *reinterpret_cast<uint4*>(kd + c * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vd + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+      mbar_arrive(&bars[1]);
     }
   }
-  cp_async_commit();
-  // Q fragments while the gather is in flight
+  // Q fragments while the rows are in flight
   const uint32_t qs_u = smem_u32(qs);
   uint32_t qa[KS][4];
   {
     const int qrow = (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
-      ldsm_x4(qs_u + sw128_offset(qrow, 2 * ks + (lane >> 4), 16), qa[ks][0], qa[ks][1], qa[ks][2],
+      ldsm_x4(qs_u + qrow * RB + (2 * ks + (lane >> 4)) * 16, qa[ks][0], qa[ks][1], qa[ks][2],
               qa[ks][3]);
   }
-  cp_async_wait<0>();
-  __syncthreads();
+  if (!mbar_wait(&bars[1], 0)) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+  __syncthreads();  // zero rows and off_s written by other threads
 
   // warp w: positions [16w, 16w + 16) of the chunk
   const int r = lane >> 2, c = lane & 3;
@@ -209,7 +230,7 @@ __global__ void __launch_bounds__(kDraftThreads)
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(ku + sw128_offset(krow, 2 * ks + ((lane >> 3) & 1), kChunk), b0, b1, b2, b3);
+      ldsm_x4(ku + krow * RB + (2 * ks + ((lane >> 3) & 1)) * 16, b0, b1, b2, b3);
       mma_16816(s[0], qa[ks], b0, b1);
       mma_16816(s[1], qa[ks], b2, b3);
     }
@@ -247,21 +268,22 @@ __global__ void __launch_bounds__(kDraftThreads)
 #pragma unroll
     for (int dp = 0; dp < DN / 2; ++dp) {
       uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vu + sw128_offset(vrow, 2 * dp + (lane >> 4), kChunk), v0, v1, v2, v3);
+      ldsm_x4_t(vu + vrow * RB + (2 * dp + (lane >> 4)) * 16, v0, v1, v2, v3);
       mma_16816(acc[2 * dp], pa, v0, v1);
       mma_16816(acc[2 * dp + 1], pa, v2, v3);
     }
   }
   __syncthreads();  // K/V tiles are free: reuse them for the warp merge
-  float* sO = reinterpret_cast<float*>(kt);  // [warps][16][HD] fp32 (32 KB at HD 128)
+  // O stash in the accumulator's own layout, rows 0..7 only (g <= 8):
+  // (warp, n-tile dn, lane) -> 2 floats, rows r = lane / 4, columns
+  // 8 dn + 2 (lane % 4) + {0, 1}; n-tiles padded to kOStride floats
+  constexpr int OS = Lay::kOStride;
+  float* sO = reinterpret_cast<float*>(kt);
   {
-    float* o = sO + (size_t)warp * 16 * HD;
 #pragma unroll
-    for (int dn = 0; dn < DN; ++dn) {
-      const int col = dn * 8 + 2 * c;
-      *reinterpret_cast<float2*>(&o[r * HD + col]) = make_float2(acc[dn][0], acc[dn][1]);
-      *reinterpret_cast<float2*>(&o[(r + 8) * HD + col]) = make_float2(acc[dn][2], acc[dn][3]);
-    }
+    for (int dn = 0; dn < DN; ++dn)
+      *reinterpret_cast<float2*>(&sO[(warp * DN + dn) * OS + lane * 2]) =
+          make_float2(acc[dn][0], acc[dn][1]);
     if (c == 0) {
       wm_s[warp][r] = m0;
       wl_s[warp][r] = l0;
@@ -292,7 +314,8 @@ __global__ void __launch_bounds__(kDraftThreads)
     const int qi = i / HD, d = i - (i / HD) * HD;
     float o = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDraftWarps; ++w) o += wm_s[w][qi] * sO[((size_t)w * 16 + qi) * HD + d];
+    for (int w = 0; w < kDraftWarps; ++w)
+      o += wm_s[w][qi] * sO[(w * DN + (d >> 3)) * OS + (qi * 4 + ((d & 7) >> 1)) * 2 + (d & 1)];
     p.part_o[slot * HD + i] = o;
   }
 }

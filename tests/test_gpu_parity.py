@@ -150,6 +150,49 @@ def test_poisoned_workspace_and_repeat():
     assert torch.equal(st.out_draft, ref_d)
 
 
+def test_draft_graph_replay_eager_and_empty_list():
+    """A captured graph of the draft steps replayed several times and eager
+    calls after it are bit-identical to the first eager run; an empty
+    attended list gives zeros."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.step import DecodeStep
+    from self_speculative_sparse_vg_gb300.workloads import make_inputs, small_spec
+    inp = make_inputs(small_spec(prefix_lens=(3000, 900)))
+    st = DecodeStep.create(inp, "cuda")
+    st.run()
+    ref = st.out_draft.clone()
+    k = st.spec.n_drafts
+    graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for t in range(1, k + 1):
+            st.draft(t, side)  # bind the side stream's arguments outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            for t in range(1, k + 1):
+                st.draft(t, side)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        st.out_draft.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(st.out_draft, ref)
+    for _ in range(2):
+        st.out_draft.fill_(float("nan"))
+        for t in range(1, k + 1):
+            st.draft(t)
+        torch.cuda.synchronize()
+        assert torch.equal(st.out_draft, ref)
+    assert P.flag(st) == 0
+    st.counts.zero_()
+    st.cur_len[0].copy_(st.tail_start)
+    st.out_draft[0].fill_(float("nan"))
+    st.draft(1)
+    torch.cuda.synchronize()
+    assert P.flag(st) == 0
+    assert (st.out_draft[0].float() == 0).all()
+
+
 def test_device_errors_flag_and_skip():
     """Bad page ids, indices, counts and lengths set the error flag; the
     offending load is skipped (no fault)."""
