@@ -72,7 +72,7 @@ enum {
    *                of s[q][i][j].
    * Order: the g * n_rows (head, row) pairs are packed as [row 0 of each
    * head][row k of each head][rows 1..k-1, head-major within a row]; each
-   * block of 16 consecutive pairs is reduced by a fixed butterfly, and the
+   * block of 32 consecutive pairs is reduced by a fixed butterfly, and the
    * blocks' sums are added in ascending block order.                       */
   VG_CAPTURE_ALL_SUM = 3
 };

@@ -6,25 +6,29 @@
 // (first draft token, bonus token) for the prefix positions.
 //
 // Design (one CTA per (KV split, KV head, sequence)):
-//  * The g query heads x R verify rows of one KV head are packed into the
-//    M dimension of warp-level bf16 tensor-core MMAs (m16n8k16, fp32
-//    accumulate), so every K/V page is read from HBM once per KV head.
-//    Row order in M: [row 0 of each head][row k of each head][rows 1..k-1],
-//    which keeps the two captured rows inside the first 16-row tile.
+//  * The g query heads x R verify rows of one KV head are packed into the M
+//    dimension of 5th-generation tensor-core MMAs (tcgen05.mma, bf16 in, fp32
+//    accumulators in tensor memory, M padded to 128), so every K/V page is
+//    read from HBM once per KV head.  Row order in M: [row 0 of each
+//    head][row k of each head][rows 1..k-1].
 //  * A producer warp streams 64-position tiles (4 pages) of K and V into a
-//    shared-memory ring with 4-D TMA loads (128-byte swizzle, evict-first
-//    L2 policy); consumers wait on mbarriers (bounded waits).
-//  * Consumer warp (mt, grp) owns rows [16 mt, 16 mt + 16) of whole 64-position
-//    tiles; the NG warp groups take alternating tiles, each keeping its own
-//    online-softmax state (8 independent MMA accumulators per warp, softmax
-//    reductions and rescales amortised over 64 positions).
-//  * Capture epilogue: the first-row-tile warps stage their 16 x 64 logits
-//    in shared memory and write either the raw two rows or their per-KV-head
-//    sum in a fixed order, with coalesced stores.  Collect-All (every row)
-//    reduces each row tile's 16 rows per column with a butterfly, hands the
-//    partial column sums to the group's first warp through shared memory
-//    (mbarrier handshakes with bounded waits), which adds them in row-tile
-//    order and stores the per-KV-head sum.
+//    shared-memory ring with 4-D TMA loads (128-byte swizzle, evict-first L2
+//    policy); the swizzled tiles are the tensor cores' K-major (K) and
+//    MN-major (V) B operands as they land.  Q and P, the A operands, live in
+//    tensor memory, so shared memory holds only the ring.
+//  * One thread issues, whichever is ready first, S = Q K^T for the next tile
+//    into one of two TMEM buffers, or O += P V for the oldest tile whose P is
+//    written, into a TMEM accumulator; the tensor cores compute the next
+//    scores during softmax and a ring stage is released as soon as its P V
+//    has run.  Completion is signalled through tcgen05.commit on mbarriers;
+//    every wait is bounded.
+//  * Softmax warps hold one packed row per lane (tcgen05.ld), so row maxima
+//    and sums need no shuffles; the exponent reference moves only when a row
+//    maximum grows by more than 2^8, and O is then rescaled in TMEM.  P goes
+//    back to tensor memory as bf16 pairs.
+//  * Capture epilogue (from the softmax warps' registers): the Collect-2 rows
+//    or their per-KV-head sum in a fixed order, or the Collect-All column
+//    sums (butterfly over each warp's rows, then warps in order).
 //  * Splits over the KV length write fp32 partials (O, m, l) to the
 //    workspace; a small merge kernel, one CTA per (output row, KV head,
 //    sequence), combines them.  It is chained with programmatic dependent
@@ -37,7 +41,6 @@
 namespace vg {
 namespace {
 
-constexpr int kTileN = 64;  // positions per pipeline stage = 4 pages
 constexpr int kMaxSplits = 256;
 
 struct VerifyParams {
@@ -70,26 +73,334 @@ __device__ __forceinline__ void row_of(int m, int g, int R, int& i, int& qi) {
   }
 }
 
-// Zero the bf16 halves of a packed pair whose positions are >= n.
-__device__ __forceinline__ uint32_t mask_pair(uint32_t v, int pos, int n) {
-  if (pos >= n) v &= 0xffff0000u;
-  if (pos + 1 >= n) v &= 0x0000ffffu;
-  return v;
-}
-
-constexpr int kVerifyMaxThreads = 256;  // <= 7 consumer warps + 1 producer
+// Thread roles: warps 0..3 are softmax warps (warp w reads TMEM lanes
+// [32 w, 32 w + 32)), warp 4 is the TMA producer, warp 5 issues the
+// tensor-core MMAs and owns the tensor memory.
+//
+// Tiles are 128 positions (8 pages), so one S = Q K^T is 8 MMAs of N = 128
+// and one O += P V is 8 MMAs of K = 16 positions: a single issuing thread
+// keeps up with HBM.  P is written back into its own S buffer (bf16 pairs in
+// the first 64 columns), which is reused by the next-but-one S only after
+// that P V has completed.
+//
+// The packed rows are replicated into CS = 4 (M <= 32), 2 (M <= 64) or 1
+// copies of the 128-row MMA tile (the padding is free): copy c occupies TMEM
+// lanes [c * 128 / CS, ...), and its warps run an independent online softmax
+// over columns [c * 128 / CS, (c + 1) * 128 / CS) of every tile, with P zero
+// elsewhere.  Each copy accumulates its own (m, l, O) over a share of the
+// positions and the copies are merged once at the end, so the per-tile
+// softmax work of a warp shrinks by CS.
+constexpr int kVTile = 128;            // positions per tile = 8 pages
+constexpr int kVerifyThreads = 192;
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kMPad = 128;             // UMMA M
+// Tensor memory columns: S double buffer (2 x 128 fp32; P aliases its first
+// 64 columns), O (<= 128 fp32), Q as the A operand (<= 64 bf16-pair columns).
+constexpr int kTmemCols = 512;
+constexpr int kSCol = 0, kOCol = 2 * kVTile, kQCol = kOCol + 128;
+constexpr float kRescaleLog2 = 8.f;    // O, l follow a new row max only past a 2^8 growth
+constexpr int kChunk = 32;             // columns a softmax pass holds in registers
+constexpr int kCapStride = kChunk + 1; // floats per staged capture row
 
 template <int HD>
-__global__ void __launch_bounds__(kVerifyMaxThreads, 1)
+struct VerifyLayout {
+  static constexpr int kTileBytes = kVTile * HD * 2;   // one of K / V: [HD/64][128 pos][128 B]
+  static constexpr int kHalfBytes = kVTile * 128;      // one 64-dim half of a tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kCapFloats = 4 * 16 * kCapStride;  // per-warp Collect-2 staging
+  static constexpr int kAllFloats = 2 * 4 * kVTile;       // Collect-All partials [slot][warp]
+  static constexpr int kBars = 12;                        // besides the ring's 2 per stage
+  static size_t bytes(int stages) {
+    return 1024 + (size_t)stages * kStageBytes + (size_t)(kCapFloats + kAllFloats) * 4 +
+           (2 * (size_t)stages + kBars) * 8 + 16;
+  }
+};
+
+struct VerifyBars {
+  uint64_t *full, *empty, *s_full, *p_full, *capfull, *capfree;
+  int stages;
+};
+
+// Softmax warp of a copy; COLS = 128 / CS columns of each tile, handled in
+// chunks of 32 (two passes over TMEM when COLS > 32: maximum, then P).
+template <int HD, int COLS>
+__device__ __forceinline__ void verify_softmax(const VerifyParams& p, const VerifyBars& bars,
+                                               uint8_t* ring, float* cap_s, float* all_s,
+                                               uint32_t tmem, int b, int h, int split, int t0,
+                                               int ntiles, int L, int warp, int lane) {
+  constexpr int CS = kVTile / COLS;       // copies
+  constexpr int QC = 4 / CS;              // warps (TMEM quadrants) per copy
+  constexpr int RPC = 32 * QC;            // rows per copy
+  constexpr int NCH = COLS / kChunk;      // chunks per tile
+  const int g = p.group, R = p.n_rows, M = p.m_rows;
+  const int NS = (M + 31) >> 5;
+  const int c = warp / QC, wq = warp % QC;  // copy, warp within the copy
+  const int nwc = (CS == 1) ? NS : QC;      // warps of this copy holding rows
+  const int col0 = c * COLS;
+  const int m = wq * 32 + lane;             // packed row of this lane
+  int lim = -1, ri = 0, rq = 0;             // last attended position, verify row, head
+  if (m < M) {
+    row_of(m, g, R, ri, rq);
+    lim = L + ri;
+  }
+  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+  const bool cap_two = wq == 0 && (p.capture_mode == VG_CAPTURE_GROUP_SUM ||
+                                   p.capture_mode == VG_CAPTURE_ROWS);
+  const bool cap_all = p.capture_mode == VG_CAPTURE_ALL_SUM;
+  const int s1 = (R > 1) ? g : 0;           // packed row of "row k, head 0"
+  const int nrows = (R > 1) ? 2 * g : g;    // captured rows
+  float* cap_w = cap_s + warp * 16 * kCapStride;
+  const int stages = bars.stages;
+  float m_used = -INFINITY, lsum = 0.f;
+  bool live = true;
+
+  for (int lt = 0; lt < ntiles; ++lt) {
+    const int sb = lt & 1, u = lt >> 1;
+    const int tile_pos = (t0 + lt) * kVTile;
+    const uint32_t sbuf = trow + kSCol + sb * kVTile;
+    if (live && !mbar_wait(&bars.s_full[sb], u & 1)) live = false;
+    tc_fence_after();
+    const int cpos = tile_pos + col0;  // position of this warp's first column
+    const int rem = lim - cpos;        // last attended column of this row among the warp's
+
+    // -------- pass 1: capture (prefix positions) and the row maximum
+    float s[kChunk];
+    float call[NCH];                   // Collect-All column sums of this lane
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      tmem_ld32(sbuf + col0 + k * kChunk, s);
+      const int kpos = cpos + k * kChunk;
+      if (kpos < L) {
+        if (cap_two) {
+          if (lane < nrows) {
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) cap_w[lane * kCapStride + j] = s[j] * p.scale;
+          }
+          __syncwarp();
+          if (kpos + lane < L) {
+            if (p.capture_mode == VG_CAPTURE_GROUP_SUM) {
+              float G = cap_w[lane] + cap_w[s1 * kCapStride + lane];
+              for (int qi = 1; qi < g; ++qi)
+                G = G + (cap_w[qi * kCapStride + lane] + cap_w[(s1 + qi) * kCapStride + lane]);
+              p.capture[((size_t)b * p.num_kv_heads + h) * p.max_prefix + kpos + lane] = G;
+            } else {
+              for (int rr = 0; rr < nrows; ++rr) {
+                const int qi = rr < g ? rr : rr - g;
+                const size_t base = ((size_t)b * p.num_q_heads + h * g + qi) * 2;
+                const float v = cap_w[rr * kCapStride + lane];
+                p.capture[(base + (rr < g ? 0 : 1)) * p.max_prefix + kpos + lane] = v;
+                if (R == 1) p.capture[(base + 1) * p.max_prefix + kpos + lane] = v;
+              }
+            }
+          }
+          __syncwarp();
+        }
+        if (cap_all) {
+          // column sums over this warp's 32 rows (rows >= M hold zeros) by
+          // recursive halving: this lane ends with column `lane` of the chunk
+          float cv[kChunk];
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j) cv[j] = s[j] * p.scale;
+#pragma unroll
+          for (int step = 0; step < 5; ++step) {
+            const int d = 16 >> step, w = (kChunk / 2) >> step;
+            const bool up = (lane & d) != 0;
+#pragma unroll
+            for (int j = 0; j < w; ++j) {
+              const float send = up ? cv[j] : cv[j + w];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, d);
+              cv[j] = (up ? cv[j + w] : cv[j]) + recv;
+            }
+          }
+          call[k] = cv[0];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j)
+        if (k * kChunk + j <= rem) mx = fmaxf(mx, s[j]);
+    }
+    if (cap_all && cpos < L) {
+      // across the copy's warps, in order, through shared memory
+      const int slot = lt & 1;
+      const int cb = c * 2 + slot;  // this copy's handshake barrier of the slot
+      float* part = all_s + slot * 4 * kVTile;
+      if (wq != 0) {
+        if (lt >= 2 && live && !mbar_wait(&bars.capfree[cb], ((lt >> 1) - 1) & 1)) live = false;
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) part[warp * kVTile + k * kChunk + lane] = call[k];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.capfull[cb]);
+      } else {
+        if (nwc > 1 && live && !mbar_wait(&bars.capfull[cb], (lt >> 1) & 1)) live = false;
+        float* dst = p.capture + ((size_t)b * p.num_kv_heads + h) * p.max_prefix + cpos;
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) {
+          float a = call[k];
+          for (int w2 = 1; w2 < nwc; ++w2) a = a + part[(warp + w2) * kVTile + k * kChunk + lane];
+          if (cpos + k * kChunk + lane < L) dst[k * kChunk + lane] = a;
+        }
+        __syncwarp();
+        if (nwc > 1 && lane == 0) mbar_arrive(&bars.capfree[cb]);
+      }
+    }
+
+    // -------- online softmax (base 2) with a lazily moved reference
+    mx *= p.scale_log2;  // scale > 0: the max commutes with it; -inf stays -inf
+    const bool need = mx > m_used + kRescaleLog2;
+    if (__any_sync(0xffffffffu, need)) {
+      const float mn = need ? mx : m_used;
+      const float corr = (mn == -INFINITY) ? 1.f : ex2(m_used - mn);
+      lsum *= corr;
+      if (lt > 0) {  // O holds P(0..t-1) V: wait for the last P.V, then scale the row
+        const int pst = (lt - 1) % stages;
+        if (live && !mbar_wait(&bars.empty[pst], ((lt - 1) / stages) & 1)) live = false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          float o[32];
+          tmem_ld32(trow + kOCol + cc * 32, o);
+          float o16[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) o16[k] = o[k] * corr;
+          tmem_st16(trow + kOCol + cc * 32, o16);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) o16[k] = o[16 + k] * corr;
+          tmem_st16(trow + kOCol + cc * 32 + 16, o16);
+        }
+        tmem_st_wait();
+      }
+      m_used = mn;
+    }
+    const float nref = -safe_ref(m_used);
+
+    // -------- pass 2: P = 2^(s - m) as bf16 pairs into the first 64 columns
+    // of this S buffer; the 16-column groups outside this warp's share are zero
+    uint32_t pk[NCH][kChunk / 2];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) {
+      if (NCH > 1) tmem_ld32(sbuf + col0 + k * kChunk, s);
+#pragma unroll
+      for (int j = 0; j < kChunk / 2; ++j) {
+        const int jj = k * kChunk + 2 * j;
+        const float p0 = jj <= rem ? ex2(fmaf(s[2 * j], p.scale_log2, nref)) : 0.f;
+        const float p1 = jj + 1 <= rem ? ex2(fmaf(s[2 * j + 1], p.scale_log2, nref)) : 0.f;
+        lsum += p0 + p1;
+        pk[k][j] = pack_bf16(p0, p1);
+      }
+    }
+    tc_fence_before();  // every read of S precedes the P writes over it
+    const uint32_t zero16[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    const int g0 = col0 / kChunk;  // this warp's first 16-column P group (32 positions each)
+#pragma unroll
+    for (int gg = 0; gg < kVTile / kChunk; ++gg)
+      if (gg < g0 || gg >= g0 + NCH) tmem_st16u(sbuf + gg * 16, zero16);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) tmem_st16u(sbuf + (g0 + k) * 16, pk[k]);
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.p_full[sb]);
+  }
+  if (!live && lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+
+  // -------- epilogue: merge the copies, then this lane's row of O
+  if (ntiles > 0 &&
+      !mbar_wait(&bars.empty[(ntiles - 1) % stages], ((ntiles - 1) / stages) & 1))
+    flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+  tc_fence_after();
+  // scratch in the idle ring, column-major so that a warp's 32 rows are 32
+  // consecutive floats: so[copy - 1][d][row], sml[copy - 1][{m, l}][row]
+  float* so = reinterpret_cast<float*>(ring);
+  float* sml = so + (CS - 1) * RPC * HD;
+  if (CS > 1 && c > 0) {
+#pragma unroll 1
+    for (int cc = 0; cc < HD / 32; ++cc) {
+      float o[32];
+      if (ntiles > 0) {
+        tmem_ld32(trow + kOCol + cc * 32, o);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] = 0.f;
+      }
+      float* d = so + ((size_t)(c - 1) * HD + cc * 32) * RPC + m;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) d[k * RPC] = o[k];
+    }
+    sml[((c - 1) * 2) * RPC + m] = m_used;
+    sml[((c - 1) * 2 + 1) * RPC + m] = lsum;
+  }
+  if (CS > 1) named_barrier_sync(1, 4 * 32);  // all four softmax warps
+  if (c > 0) return;
+  // weights of the copies relative to the largest reference
+  float mxr = m_used;
+  for (int c2 = 1; c2 < CS; ++c2) mxr = fmaxf(mxr, sml[((c2 - 1) * 2) * RPC + m]);
+  const float ref = safe_ref(mxr);
+  const float w0 = m_used == -INFINITY ? 0.f : ex2(m_used - ref);
+  float wc[CS > 1 ? CS - 1 : 1];
+  float lt_all = w0 * lsum;
+#pragma unroll
+  for (int c2 = 1; c2 < CS; ++c2) {
+    const float mc = sml[((c2 - 1) * 2) * RPC + m];
+    const float lc = sml[((c2 - 1) * 2 + 1) * RPC + m];
+    wc[c2 - 1] = mc == -INFINITY ? 0.f : ex2(mc - ref);
+    lt_all += wc[c2 - 1] * lc;
+  }
+  const size_t bh = (size_t)b * p.num_kv_heads + h;
+  const float inv = lt_all > 0.f ? 1.f / lt_all : 0.f;
+#pragma unroll 1
+  for (int cc = 0; cc < HD / 32; ++cc) {
+    float o[32];
+    if (ntiles > 0) {
+      tmem_ld32(trow + kOCol + cc * 32, o);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) o[k] = 0.f;
+    }
+    if (m < M) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) o[k] *= w0;
+#pragma unroll
+      for (int c2 = 1; c2 < CS; ++c2) {
+        const float* src = so + ((size_t)(c2 - 1) * HD + cc * 32) * RPC + m;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] += wc[c2 - 1] * src[k * RPC];
+      }
+      if (p.splits == 1) {
+        __nv_bfloat16* dst =
+            p.out + ((size_t)(b * R + ri) * p.num_q_heads + h * g + rq) * HD + cc * 32;
+#pragma unroll
+        for (int k = 0; k < 32; k += 8) {
+          uint4 w;
+          w.x = pack_bf16(o[k] * inv, o[k + 1] * inv);
+          w.y = pack_bf16(o[k + 2] * inv, o[k + 3] * inv);
+          w.z = pack_bf16(o[k + 4] * inv, o[k + 5] * inv);
+          w.w = pack_bf16(o[k + 6] * inv, o[k + 7] * inv);
+          *reinterpret_cast<uint4*>(dst + k) = w;
+        }
+      } else {
+        float* dst = p.part_o + ((bh * p.splits + split) * M + m) * HD + cc * 32;
+#pragma unroll
+        for (int k = 0; k < 32; k += 4)
+          *reinterpret_cast<float4*>(dst + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+      }
+    }
+  }
+  if (m < M && p.splits > 1) {
+    float* ml = p.part_ml + ((bh * p.splits + split) * M + m) * 2;
+    ml[0] = mxr;
+    ml[1] = lt_all;
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kVerifyThreads, 1)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const VerifyParams p) {
-  constexpr int NT = kTileN / 8;  // S n-tiles per warp: a warp owns a whole 64-position tile
+  using Lay = VerifyLayout<HD>;
   constexpr int KS = HD / 16;     // k-steps of Q K^T
-  constexpr int DN = HD / 8;      // O n-tiles
-  constexpr int CH = HD / 8;      // 16-byte chunks per row
-  constexpr int kTileBytes = kTileN * HD * 2;  // one of K / V
-  constexpr int kStageBytes = 2 * kTileBytes;
-  constexpr int kCapStride = 72;  // floats per row of a warp's capture staging tile
+  constexpr int kTileBytes = Lay::kTileBytes;
+  constexpr int kStageBytes = Lay::kStageBytes;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -97,56 +408,110 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.group, R = p.n_rows, M = p.m_rows;
-  const int MT = p.m_tiles, NG = p.groups;
-  const int n_cons = MT * NG;
-  const int Mpad = MT * 16;
+  const int NS = (M + 31) >> 5;
+  const int CS = M <= 32 ? 4 : (M <= 64 ? 2 : 1);  // row copies
+  const int RPC = kMPad / CS;                        // TMEM lanes per copy
+  const int NAW = CS == 1 ? NS : 4;                  // softmax warps at work
   const int stages = p.stages;
 
   uint8_t* ring = smem;
-  uint8_t* qs = ring + stages * kStageBytes;
-  float* cbuf = reinterpret_cast<float*>(qs + Mpad * HD * 2);
-  float* cpart = cbuf + NG * 16 * kCapStride;  // Collect-All partials [NG][2][MT][64]
-  uint64_t* full = reinterpret_cast<uint64_t*>(cpart + NG * 2 * MT * kTileN);
-  uint64_t* empty = full + stages;
-  uint64_t* capfull = empty + stages;  // [NG][2]: partials of a slot written
-  uint64_t* capfree = capfull + 2 * NG;  // [NG][2]: a slot read by the group's first warp
+  float* cap_s = reinterpret_cast<float*>(ring + (size_t)stages * kStageBytes);
+  float* all_s = cap_s + Lay::kCapFloats;
+  VerifyBars bars;
+  bars.stages = stages;
+  bars.full = reinterpret_cast<uint64_t*>(all_s + Lay::kAllFloats);
+  bars.empty = bars.full + stages;    // P(t) V(t) done: ring stage, S and P buffer free
+  bars.s_full = bars.empty + stages;  // S of a buffer computed (tensor-core commit)
+  bars.p_full = bars.s_full + 2;      // P of a buffer written by every softmax warp
+  bars.capfull = bars.p_full + 2;     // [copy][slot]: Collect-All partials written
+  bars.capfree = bars.capfull + 4;    // [copy][slot]: Collect-All slot read
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars.capfree + 4);
 
   // programmatic dependent launch: inputs may come from the previous kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
+  // The producer reads the page ids of its first 4 tiles while the length is
+  // still in flight (within the page-table row; ids past the sequence are
+  // dropped once the length is known).
+  constexpr int kPagesPerTile = kVTile / kPageSize;  // 8
+  int pre_id = -1;
+  if (warp == kProducerWarp) {
+    const int lp = split * p.tiles_per_split * kPagesPerTile + lane;
+    if (lp < p.max_pages_per_seq) pre_id = p.page_table[(size_t)b * p.max_pages_per_seq + lp];
+  }
   const int L = p.prefix_lens[b];
   const int n_b = L + R;
   if (L < 1 || L > p.max_prefix || (n_b + kPageSize - 1) / kPageSize > p.max_pages_per_seq) {
     if (threadIdx.x == 0 && split == 0 && h == 0) flag_error(p.error_flag, VG_DEVERR_LENGTH);
     return;  // uniform for every CTA of this sequence
   }
-  const int tiles_b = (n_b + kTileN - 1) / kTileN;
+  const int tiles_b = (n_b + kVTile - 1) / kVTile;
   const int t0 = split * p.tiles_per_split;
   const int ntiles = max(0, min(t0 + p.tiles_per_split, tiles_b) - t0);
   const int npages_b = (n_b + kPageSize - 1) / kPageSize;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MT);  // a tile is consumed by the MT warps of one group
+      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.empty[s], 1);
     }
-    for (int s = 0; s < 2 * NG; ++s) {
-      mbar_init(&capfull[s], MT > 1 ? MT - 1 : 1);
-      mbar_init(&capfree[s], 1);
+    const int nwc = CS == 1 ? NS : 4 / CS;  // warps per copy holding rows
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.s_full[s], 1);
+      mbar_init(&bars.p_full[s], NAW);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars.capfull[s], nwc > 1 ? nwc - 1 : 1);
+      mbar_init(&bars.capfree[s], 1);
     }
     fence_barrier_init();
   }
-  __syncthreads();  // barriers initialised: the producer may start at once
-
-  float mrun0 = -INFINITY, mrun1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float acc[DN][4];
+  if (warp == kMmaWarp) tmem_alloc(tmem_holder, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // Q is handed from the softmax warps to the MMA warp through named barrier
+  // 2 (warps 0-3 and 5); the producer starts its loads at once
+  constexpr int kQReadyBar = 2, kQReadyThreads = 5 * 32;
+  if (warp < 4) {
+    // Q -> tensor memory (A operand): lane c * RPC + m holds packed row m of
+    // copy c, every other lane zero (its logits are exactly zero)
+    const int row = 32 * warp + lane;
+    const int cp = row / RPC, mm = row - cp * RPC;
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint4* src = nullptr;
+    if (cp < CS && mm < M) {
+      int i, qi;
+      row_of(mm, g, R, i, qi);
+      src = reinterpret_cast<const uint4*>(p.q + ((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD);
+    }
 #pragma unroll
-  for (int dn = 0; dn < DN; ++dn) acc[dn][0] = acc[dn][1] = acc[dn][2] = acc[dn][3] = 0.f;
+    for (int half = 0; half < HD / 64; ++half) {
+      uint32_t v[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 x = src ? src[half * 8 + k] : make_uint4(0, 0, 0, 0);
+        v[4 * k] = x.x;
+        v[4 * k + 1] = x.y;
+        v[4 * k + 2] = x.z;
+        v[4 * k + 3] = x.w;
+      }
+      tmem_st32u(trow + kQCol + half * 32, v);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    named_barrier_sync(kQReadyBar, kQReadyThreads);
+  } else if (warp == kMmaWarp) {
+    named_barrier_sync(kQReadyBar, kQReadyThreads);
+    tc_fence_after();
+  }
 
-  if (warp == n_cons) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------- producer
-    // The warp fetches the page ids of 8 tiles (32 ids, one per lane) in one
-    // round trip; lane 0 then issues the tiles' TMA loads as stages free up.
+    // The warp fetches the page ids of 4 tiles (32 ids, one per lane) in one
+    // round trip; then each lane issues one TMA box (16 positions x 64 dims
+    // of K or V) of a tile as its ring stage frees up.
     if (ntiles > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&tmk);
@@ -155,12 +520,12 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
       const uint64_t pol = l2_policy_evict_first();
       int my_id = p.num_pages;
       for (int lt = 0; lt < ntiles; ++lt) {
-        if ((lt & 7) == 0) {
-          const int lt_l = lt + (lane >> 2);
-          const int lp = (t0 + lt_l) * (kTileN / kPageSize) + (lane & 3);
+        if ((lt & 3) == 0) {
+          const int lt_l = lt + (lane >> 3);
+          const int lp = (t0 + lt_l) * kPagesPerTile + (lane & 7);
           my_id = p.num_pages;  // out of range: TMA fills zeros
           if (lt_l < ntiles && lp < npages_b) {
-            const int e = p.page_table[(size_t)b * p.max_pages_per_seq + lp];
+            const int e = lt == 0 ? pre_id : p.page_table[(size_t)b * p.max_pages_per_seq + lp];
             if (e >= 0 && e < p.num_pages)
               my_id = e;
             else
@@ -169,354 +534,101 @@ __global__ void __launch_bounds__(kVerifyMaxThreads, 1)
         }
         const int st = lt % stages;
         int go = 1;
-        if (lane == 0 && lt >= stages) go = mbar_wait(&empty[st], ((lt / stages) - 1) & 1);
+        if (lane == 0 && lt >= stages) go = mbar_wait(&bars.empty[st], ((lt / stages) - 1) & 1);
         go = __shfl_sync(0xffffffffu, go, 0);
         if (!go) {
           if (lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
           break;
         }
-        // one TMA box (16 positions x 64 dims) per lane: page pi, half dh, K or V
-        constexpr int kBoxes = (kTileN / kPageSize) * (HD / 64) * 2;
+        // lane -> page pi, half dh, K or V
+        constexpr int kBoxes = kPagesPerTile * (HD / 64) * 2;
         const int pi = lane / ((HD / 64) * 2), dh = (lane >> 1) & (HD / 64 - 1), kv = lane & 1;
-        const int id = __shfl_sync(0xffffffffu, my_id, (lt & 7) * 4 + (pi & 3));
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], kStageBytes);
+        const int id = __shfl_sync(0xffffffffu, my_id, (lt & 3) * 8 + (pi & 7));
+        if (lane == 0) mbar_arrive_expect_tx(&bars.full[st], kStageBytes);
         __syncwarp();
         if (lane < kBoxes) {
-          uint8_t* dst = ring + st * kStageBytes + kv * kTileBytes + dh * kTileN * 128 +
+          uint8_t* dst = ring + st * kStageBytes + kv * kTileBytes + dh * Lay::kHalfBytes +
                          pi * kPageSize * 128;
-          tma_load_4d(dst, kv ? &tmv : &tmk, &full[st], dh * 64, 0, h, id, pol);
+          tma_load_4d(dst, kv ? &tmv : &tmk, &bars.full[st], dh * 64, 0, h, id, pol);
         }
         __syncwarp();
       }
     }
-  } else {
-    // ---------------------------------------------------------- consumers
-    // Q rows of this KV head -> shared (same swizzled layout as K), padding
-    // zero; only the consumer warps wait for it (named barrier 1).
-    for (int idx = threadIdx.x; idx < Mpad * CH; idx += n_cons * 32) {
-      const int row = idx / CH, ch = idx - (idx / CH) * CH;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (row < M) {
-        int i, qi;
-        row_of(row, g, R, i, qi);
-        const size_t off = ((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD + ch * 8;
-        v = *reinterpret_cast<const uint4*>(p.q + off);
-      }
-      *reinterpret_cast<uint4*>(qs + sw128_offset(row, ch, Mpad)) = v;
-    }
-    named_barrier_sync(1, n_cons * 32);
-    // warp (mt, grp): rows [16 mt, 16 mt + 16) of tiles grp, grp + NG, ...
-    // The ring depth is a multiple of NG, so a stage's previous phase was
-    // consumed by this same group and a parity wait can never see it stale.
-    const int mt = warp % MT, grp = warp / MT;
-    const int r = lane >> 2, c = lane & 3;
-    const int m0 = mt * 16 + r, m1 = m0 + 8;
-    int lim0 = n_b - 1, lim1 = n_b - 1;  // last attended position of each row
-    {
-      int i, qi;
-      if (m0 < M) { row_of(m0, g, R, i, qi); lim0 = L + i; }
-      if (m1 < M) { row_of(m1, g, R, i, qi); lim1 = L + i; }
-    }
-    const uint32_t qs_u = smem_u32(qs);
-    uint32_t qa[KS][4];
-    const int qrow = mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issue
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t ring_u = smem_u32(ring);
+      constexpr uint32_t id_qk = umma_idesc_bf16(kMPad, kVTile, 0, 0);
+      constexpr uint32_t id_pv = umma_idesc_bf16(kMPad, HD, 0, 1);
+      // Issue whichever is ready: S(t) = Q K(t)^T (needs tile t and P(t - 2) V
+      // done, which frees its S buffer) or O += P(t) V(t) (needs P(t)).
+      int nq = 0, np = 0;
+      bool live = true;
+      uint64_t last = global_timer_ns();
+      while (np < ntiles) {
+        bool moved = false;
+        if (nq < ntiles) {
+          const int st = nq % stages, sb = nq & 1;
+          if (mbar_test_wait(&bars.full[st], (nq / stages) & 1) &&
+              (nq < 2 || mbar_test_wait(&bars.empty[(nq - 2) % stages], ((nq - 2) / stages) & 1))) {
+            tc_fence_after();
+            const uint32_t kb = ring_u + st * kStageBytes;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
-      ldsm_x4(qs_u + sw128_offset(qrow, 2 * ks + (lane >> 4), Mpad), qa[ks][0], qa[ks][1],
-              qa[ks][2], qa[ks][3]);
-    const bool cap_warp =
-        (mt == 0) && (p.capture_mode == VG_CAPTURE_GROUP_SUM || p.capture_mode == VG_CAPTURE_ROWS);
-    const bool cap_all = p.capture_mode == VG_CAPTURE_ALL_SUM;
-    bool cap_live = true;  // false after a capture handshake timed out: wait no more
-    float* cb = cbuf + grp * 16 * kCapStride;
-    const uint32_t ring_u = smem_u32(ring);
-    const int krow = (lane & 7) + ((lane >> 4) << 3);       // K ldmatrix row within 16
-    const int kchk = (lane >> 3) & 1;                        // K ldmatrix chunk offset
-    const int vrow = (lane & 7) + (((lane >> 3) & 1) << 3);  // V ldmatrix.trans row within 16
-    const int vchk = lane >> 4;                              // V ldmatrix.trans chunk offset
-
-    for (int lt = grp; lt < ntiles; lt += NG) {
-      const int st = lt % stages;
-      if (!mbar_wait(&full[st], (lt / stages) & 1)) {
-        flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-        break;
-      }
-      const uint32_t kt = ring_u + st * kStageBytes, vt = kt + kTileBytes;
-      const int tile_pos = (t0 + lt) * kTileN;
-
-      // S = Q K^T for 16 rows x 64 positions: 8 independent accumulators
-      float s[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-        for (int np = 0; np < NT / 2; ++np) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kt + sw128_offset(np * 16 + krow, 2 * ks + kchk, kTileN), b0, b1, b2, b3);
-          mma_16816(s[2 * np], qa[ks], b0, b1);
-          mma_16816(s[2 * np + 1], qa[ks], b2, b3);
-        }
-      }
-
-      // Collect-2-Query capture (prefix positions only)
-      if (cap_warp && tile_pos < L) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int col = nt * 8 + 2 * c;
-          *reinterpret_cast<float2*>(&cb[r * kCapStride + col]) =
-              make_float2(s[nt][0] * p.scale, s[nt][1] * p.scale);
-          *reinterpret_cast<float2*>(&cb[(r + 8) * kCapStride + col]) =
-              make_float2(s[nt][2] * p.scale, s[nt][3] * p.scale);
-        }
-        __syncwarp();
-        const int s1 = (R > 1) ? g : 0;
-#pragma unroll
-        for (int jj = 0; jj < kTileN / 32; ++jj) {
-          const int j = jj * 32 + lane;
-          const int pos = tile_pos + j;
-          if (pos < L) {
-            if (p.capture_mode == VG_CAPTURE_GROUP_SUM) {
-              float G = cb[j] + cb[s1 * kCapStride + j];
-              for (int qi = 1; qi < g; ++qi)
-                G = G + (cb[qi * kCapStride + j] + cb[(s1 + qi) * kCapStride + j]);
-              p.capture[((size_t)b * p.num_kv_heads + h) * p.max_prefix + pos] = G;
-            } else {
-              for (int qi = 0; qi < g; ++qi) {
-                const size_t base = ((size_t)b * p.num_q_heads + h * g + qi) * 2;
-                p.capture[base * p.max_prefix + pos] = cb[qi * kCapStride + j];
-                p.capture[(base + 1) * p.max_prefix + pos] = cb[(s1 + qi) * kCapStride + j];
-              }
+            for (int ks = 0; ks < KS; ++ks) {
+              const uint64_t bd =
+                  umma_smem_desc(kb + (ks >> 2) * Lay::kHalfBytes + (ks & 3) * 32, 16, 1024);
+              umma_bf16_ts(tmem + kSCol + sb * kVTile, tmem + kQCol + ks * 8, bd, id_qk, ks > 0);
             }
+            umma_commit(&bars.s_full[sb]);
+            ++nq;
+            moved = true;
           }
         }
-        __syncwarp();
-      }
-
-      // Collect-All-Query capture: sum of every row of the tile's columns
-      if (cap_all && tile_pos < L) {
-        const int use_n = (lt - grp) / NG;  // this group's tile counter
-        const int slot = use_n & 1, use = use_n >> 1;
-        float* part = cpart + (size_t)(grp * 2 + slot) * MT * kTileN;
-        float cs[NT][2];
+        if (np < nq) {
+          const int st = np % stages, sb = np & 1;
+          if (mbar_test_wait(&bars.p_full[sb], (np >> 1) & 1)) {
+            tc_fence_after();
+            const uint32_t vb = ring_u + st * kStageBytes + kTileBytes;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            // rows r and r + 8 of this warp, then the 8 row pairs (lanes
-            // with the same c) by a fixed butterfly; padded rows hold zeros
-            float v = s[nt][e] * p.scale + s[nt][2 + e] * p.scale;
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            v += __shfl_xor_sync(0xffffffffu, v, 8);
-            v += __shfl_xor_sync(0xffffffffu, v, 16);
-            cs[nt][e] = v;
-          }
-        }
-        if (mt != 0 && use > 0 && cap_live &&
-            !mbar_wait(&capfree[grp * 2 + slot], (use - 1) & 1)) {
-          flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-          cap_live = false;
-        }
-        if (r == 0) {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            *reinterpret_cast<float2*>(&part[mt * kTileN + nt * 8 + 2 * c]) =
-                make_float2(cs[nt][0], cs[nt][1]);
-        }
-        __syncwarp();
-        if (mt != 0) {
-          if (lane == 0) mbar_arrive(&capfull[grp * 2 + slot]);
-        } else {
-          if (MT > 1 && cap_live && !mbar_wait(&capfull[grp * 2 + slot], use & 1)) {
-            flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-            cap_live = false;
-          }
-          if (cap_live) {
-#pragma unroll
-            for (int jj = 0; jj < kTileN / 32; ++jj) {
-              const int j = jj * 32 + lane;
-              const int pos = tile_pos + j;
-              if (pos < L) {
-                float A = part[j];
-                for (int m2 = 1; m2 < MT; ++m2) A = A + part[m2 * kTileN + j];
-                p.capture[((size_t)b * p.num_kv_heads + h) * p.max_prefix + pos] = A;
-              }
+            for (int ks = 0; ks < kVTile / 16; ++ks) {
+              // V is MN-major: 64-dim blocks one half-tile apart, 8-position groups 1 KB apart
+              const uint64_t bd = umma_smem_desc(vb + ks * 16 * 128, Lay::kHalfBytes, 1024);
+              umma_bf16_ts(tmem + kOCol, tmem + kSCol + sb * kVTile + ks * 8, bd, id_pv,
+                           (np > 0 || ks > 0));
             }
-          }
-          __syncwarp();
-          if (MT > 1 && lane == 0) mbar_arrive(&capfree[grp * 2 + slot]);
-        }
-      }
-
-      // online softmax (base 2); only the last tiles need the causal mask
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-      if (tile_pos + kTileN <= L + 1) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            s[nt][e] *= p.scale_log2;
-            s[nt][2 + e] *= p.scale_log2;
-            mx0 = fmaxf(mx0, s[nt][e]);
-            mx1 = fmaxf(mx1, s[nt][2 + e]);
+            umma_commit(&bars.empty[st]);
+            ++np;
+            moved = true;
           }
         }
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int pos = tile_pos + nt * 8 + 2 * c + e;
-            s[nt][e] = (pos <= lim0) ? s[nt][e] * p.scale_log2 : -INFINITY;
-            s[nt][2 + e] = (pos <= lim1) ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
-            mx0 = fmaxf(mx0, s[nt][e]);
-            mx1 = fmaxf(mx1, s[nt][2 + e]);
-          }
+        if (moved) {
+          last = global_timer_ns();
+        } else if (global_timer_ns() - last > kWaitLimitNs) {
+          live = false;
+          break;
         }
       }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(mrun0, mx0), mn1 = fmaxf(mrun1, mx1);
-      const float ref0 = safe_ref(mn0), ref1 = safe_ref(mn1);
-      const float corr0 = ex2(mrun0 - ref0), corr1 = ex2(mrun1 - ref1);
-      mrun0 = mn0;
-      mrun1 = mn1;
-      l0 *= corr0;
-      l1 *= corr1;
-      if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
-#pragma unroll
-        for (int dn = 0; dn < DN; ++dn) {
-          acc[dn][0] *= corr0;
-          acc[dn][1] *= corr0;
-          acc[dn][2] *= corr1;
-          acc[dn][3] *= corr1;
-        }
-      }
-      uint32_t pa[NT / 2][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float p00 = ex2(s[nt][0] - ref0), p01 = ex2(s[nt][1] - ref0);
-        const float p10 = ex2(s[nt][2] - ref1), p11 = ex2(s[nt][3] - ref1);
-        l0 += p00 + p01;
-        l1 += p10 + p11;
-        pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(p00, p01);
-        pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(p10, p11);
-      }
-
-      // O += P V
-      const bool ragged = tile_pos + kTileN > n_b;
-#pragma unroll
-      for (int kk = 0; kk < NT / 2; ++kk) {
-        const int posA = tile_pos + kk * 16 + 2 * c;
-#pragma unroll
-        for (int dp = 0; dp < DN / 2; ++dp) {
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_t(vt + sw128_offset(kk * 16 + vrow, 2 * dp + vchk, kTileN), v0, v1, v2, v3);
-          if (ragged) {
-            v0 = mask_pair(v0, posA, n_b);
-            v2 = mask_pair(v2, posA, n_b);
-            v1 = mask_pair(v1, posA + 8, n_b);
-            v3 = mask_pair(v3, posA + 8, n_b);
-          }
-          mma_16816(acc[2 * dp], pa[kk], v0, v1);
-          mma_16816(acc[2 * dp + 1], pa[kk], v2, v3);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
+      // the last P.V has finished before the tensor memory is released
+      if (live &&
+          !mbar_wait(&bars.empty[(ntiles - 1) % stages], ((ntiles - 1) / stages) & 1))
+        live = false;
+      if (!live) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
     }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    __syncwarp();
+  } else if (warp < NAW) {
+    // ---------------------------------------------------------- softmax
+    if (CS == 4)
+      verify_softmax<HD, 32>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
+    else if (CS == 2)
+      verify_softmax<HD, 64>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
+    else
+      verify_softmax<HD, 128>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
   }
-  __syncthreads();  // ring idle: every issued load was consumed
-
-  // ---------------------------------------------- merge the NG tile groups
-  float* sO = reinterpret_cast<float*>(ring);          // [n_cons][16][HD]
-  float* sML = sO + (size_t)n_cons * 16 * HD;          // [n_cons][16][2]
-  float* sW = sML + (size_t)n_cons * 16 * 2;           // [M][NG]
-  float* sRow = sW + (size_t)Mpad * NG;                // [M][2]
-  if (warp < n_cons) {
-    float* o = sO + (size_t)warp * 16 * HD;
-    const int r = lane >> 2, c = lane & 3;
-#pragma unroll
-    for (int dn = 0; dn < DN; ++dn) {
-      const int col = dn * 8 + 2 * c;
-      *reinterpret_cast<float2*>(&o[r * HD + col]) = make_float2(acc[dn][0], acc[dn][1]);
-      *reinterpret_cast<float2*>(&o[(r + 8) * HD + col]) = make_float2(acc[dn][2], acc[dn][3]);
-    }
-    if (c == 0) {
-      sML[(warp * 16 + r) * 2] = mrun0;
-      sML[(warp * 16 + r) * 2 + 1] = l0;
-      sML[(warp * 16 + r + 8) * 2] = mrun1;
-      sML[(warp * 16 + r + 8) * 2 + 1] = l1;
-    }
-  }
-  __syncthreads();
-  for (int m = threadIdx.x; m < M; m += blockDim.x) {
-    const int mt = m >> 4, rr = m & 15;
-    float mx = -INFINITY;
-    for (int gq = 0; gq < NG; ++gq) mx = fmaxf(mx, sML[((gq * MT + mt) * 16 + rr) * 2]);
-    const float ref = safe_ref(mx);
-    float lt = 0.f;
-    for (int gq = 0; gq < NG; ++gq) {
-      const float w = ex2(sML[((gq * MT + mt) * 16 + rr) * 2] - ref);
-      sW[m * NG + gq] = w;
-      lt += w * sML[((gq * MT + mt) * 16 + rr) * 2 + 1];
-    }
-    sRow[m * 2] = mx;
-    sRow[m * 2 + 1] = lt;
-    if (p.splits == 1) {
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      for (int gq = 0; gq < NG; ++gq) sW[m * NG + gq] *= inv;
-    }
-  }
-  __syncthreads();
-
-  const size_t bh = (size_t)b * p.num_kv_heads + h;
-  if (p.splits == 1) {
-    for (int e = threadIdx.x; e < M * (HD / 2); e += blockDim.x) {
-      const int m = e / (HD / 2), d = (e - m * (HD / 2)) * 2;
-      const int mt = m >> 4, rr = m & 15;
-      float o0 = 0.f, o1 = 0.f;
-      for (int gq = 0; gq < NG; ++gq) {
-        const float w = sW[m * NG + gq];
-        const float2 v =
-            *reinterpret_cast<const float2*>(&sO[((size_t)(gq * MT + mt) * 16 + rr) * HD + d]);
-        o0 += w * v.x;
-        o1 += w * v.y;
-      }
-      int i, qi;
-      row_of(m, g, R, i, qi);
-      *reinterpret_cast<__nv_bfloat162*>(
-          &p.out[((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD + d]) =
-          __floats2bfloat162_rn(o0, o1);
-    }
-    return;
-  }
-
-  // split-K: publish the partial; verify_merge_kernel combines the splits
-  float* po = p.part_o + ((bh * p.splits + split) * M) * HD;
-  float* pml = p.part_ml + (bh * p.splits + split) * M * 2;
-  for (int e = threadIdx.x; e < M * (HD / 2); e += blockDim.x) {
-    const int m = e / (HD / 2), d = (e - m * (HD / 2)) * 2;
-    const int mt = m >> 4, rr = m & 15;
-    float o0 = 0.f, o1 = 0.f;
-    for (int gq = 0; gq < NG; ++gq) {
-      const float w = sW[m * NG + gq];
-      const float2 v =
-          *reinterpret_cast<const float2*>(&sO[((size_t)(gq * MT + mt) * 16 + rr) * HD + d]);
-      o0 += w * v.x;
-      o1 += w * v.y;
-    }
-    *reinterpret_cast<float2*>(&po[(size_t)m * HD + d]) = make_float2(o0, o1);
-  }
-  for (int m = threadIdx.x; m < M; m += blockDim.x) {
-    pml[m * 2] = sRow[m * 2];
-    pml[m * 2 + 1] = sRow[m * 2 + 1];
+  tc_fence_before();
+  __syncthreads();  // every TMEM access and every MMA of this CTA is done
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -558,9 +670,8 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   pl->hd = head_dim;
   pl->m_rows = g * n_rows;
   pl->m_tiles = ceil_div(pl->m_rows, 16);
-  // tile groups working on alternating tiles; consumers + producer <= 8 warps
-  pl->groups = pl->m_tiles <= 2 ? 3 : (pl->m_tiles <= 3 ? 2 : 1);
-  const int tiles = ceil_div(max_prefix + n_rows, kTileN);
+  pl->groups = 1;
+  const int tiles = ceil_div(max_prefix + n_rows, kVTile);
   int tps;
   if (num_splits > 0) {
     tps = ceil_div(tiles, std::min(num_splits, tiles));
@@ -569,28 +680,17 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
     const int sms = device_sm_count();
     int splits = std::max(1, sms / pairs);
     tps = ceil_div(tiles, splits);
-    if (batch > 1) tps = std::min(tps, 32);  // ragged lengths: small chunks balance SMs
-    tps = std::max(tps, std::min(tiles, 4));
+    if (batch > 1) tps = std::min(tps, 16);  // ragged lengths: small chunks balance SMs
+    tps = std::max(tps, std::min(tiles, 2));
   }
   if (ceil_div(tiles, tps) > kMaxSplits) tps = ceil_div(tiles, kMaxSplits);
   pl->tiles_per_split = tps;
   pl->splits = ceil_div(tiles, tps);
-  const int stage_bytes = 2 * kTileN * head_dim * 2;
-  const int n_cons = pl->m_tiles * pl->groups;
-  const int mpad = pl->m_tiles * 16;
   auto smem_for = [&](int stages) {
-    return 1024 + (size_t)stages * stage_bytes + (size_t)mpad * head_dim * 2 +
-           (size_t)pl->groups * 16 * 72 * 4 + (size_t)pl->groups * 2 * pl->m_tiles * kTileN * 4 +
-           2 * stages * 8 + 4 * pl->groups * 8 + 16;
+    return head_dim == 128 ? VerifyLayout<128>::bytes(stages) : VerifyLayout<64>::bytes(stages);
   };
-  // ring depth: a multiple of the group count (see the consumer loop), 192 KB
-  // at head_dim 128, shrunk if the whole layout would not fit
-  int stages = (head_dim == 128 ? 6 : 12);
-  while (stages > pl->groups && smem_for(stages) > 227 * 1024) stages -= pl->groups;
-  // the ring is reused after the main loop for the merge of the tile groups
-  const size_t merge_bytes =
-      (size_t)n_cons * 16 * (head_dim + 2) * 4 + (size_t)mpad * (pl->groups + 2) * 4;
-  if ((size_t)stages * stage_bytes < merge_bytes) return false;
+  int stages = (head_dim == 128 ? 3 : 6);
+  while (stages > 2 && smem_for(stages) > 227 * 1024) --stages;
   pl->stages = stages;
   pl->smem_bytes = smem_for(stages);
   const size_t o_bytes = (size_t)batch * num_kv_heads * pl->splits * pl->m_rows * head_dim * 4;
@@ -617,7 +717,7 @@ cudaError_t launch_verify(const VerifyPlan& pl, const CUtensorMap& tk, const CUt
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t vcfg = {};
   vcfg.gridDim = grid;
-  vcfg.blockDim = dim3((pl.m_tiles * pl.groups + 1) * 32, 1, 1);
+  vcfg.blockDim = dim3(kVerifyThreads, 1, 1);
   vcfg.dynamicSmemBytes = pl.smem_bytes;
   vcfg.stream = stream;
   vcfg.attrs = pdl;
