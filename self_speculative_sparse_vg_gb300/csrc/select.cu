@@ -93,30 +93,6 @@ __device__ __forceinline__ float row_score(const SelectParams& p, int b, int row
   return acc;
 }
 
-// Exclusive block-wide count of a per-thread flag; *total = block sum.
-__device__ __forceinline__ int block_excl_count(bool f, int* wb, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const unsigned bal = __ballot_sync(0xffffffffu, f);
-  if (lane == 0) wb[warp] = __popc(bal);
-  __syncthreads();
-  if (warp == 0) {
-    const int v = lane < nw ? wb[lane] : 0;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    wb[32 + lane] = incl - v;
-    if (lane == 31) wb[64] = incl;
-  }
-  __syncthreads();
-  const int r = wb[32 + warp] + __popc(bal & ((1u << lane) - 1u));
-  *total = wb[64];
-  __syncthreads();
-  return r;
-}
-
 // Score pass, spread over many CTAs (one position per thread): the fixed-order
 // fp32 score of every prefix position, stored as its order-preserving key.
 constexpr int kScoreThreads = 256;
@@ -142,7 +118,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   __shared__ uint32_t tot_s[256];
   __shared__ int cnt[2];    // this CTA's candidate keys > T and == T
   __shared__ int ctl[5];    // digit, remaining k, gt_before, eq_before, boundary-bin count
-  __shared__ int wb[96];
+  __shared__ int wb[160];
   extern __shared__ __align__(16) uint32_t keys[];  // [slice]
 
   // programmatic dependent launch: the capture comes from the previous kernel
@@ -241,29 +217,47 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   // positions first.
   const uint32_t T = prefix;
 
-  // ---- per-CTA counts of > T and == T, exclusive prefix over lower ranks
-  if (tid < 2) cnt[tid] = 0;
-  __syncthreads();
+  // ---- kept keys: every (key & mask) > T, and the first krem with
+  // (key & mask) == T in position order, written to their sorted slots.
+  // Warp w owns the contiguous key range [w * 32 * per, (w + 1) * 32 * per)
+  // of this CTA's slice, read 32 at a time; counts go through ballots, and
+  // the warps are ordered by one exclusive scan per quantity.
+  const int per = (n_loc + kSelThreads - 1) / kSelThreads;  // keys per lane
+  const int wid = tid >> 5;
+  const int wbase = wid * 32 * per;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int gt_w = 0, eq_w = 0;
   if (p.top_k > 0) {
-    int gt = 0, eq = 0;
-    for (int j = tid; j < n_loc; j += blockDim.x) {
+    for (int i = 0; i < per; ++i) {
+      const int j = wbase + i * 32 + lane;
       const int pos = lo + j;
-      if (pos >= c_lo && pos < c_hi) {
-        const uint32_t k = keys[j] & mask;
-        gt += k > T;
-        eq += k == T;
-      }
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      gt += __shfl_xor_sync(0xffffffffu, gt, o);
-      eq += __shfl_xor_sync(0xffffffffu, eq, o);
-    }
-    if (lane == 0) {
-      atomicAdd(&cnt[0], gt);
-      atomicAdd(&cnt[1], eq);
+      const bool in = j < n_loc && pos >= c_lo && pos < c_hi;
+      const uint32_t k = in ? (keys[j] & mask) : 0u;
+      gt_w += __popc(__ballot_sync(0xffffffffu, in && k > T));
+      eq_w += __popc(__ballot_sync(0xffffffffu, in && k == T));
     }
   }
-  cluster.sync();
+  if (lane == 0) {
+    wb[wid] = eq_w;
+    wb[32 + wid] = gt_w;
+  }
+  __syncthreads();
+  if (wid == 0) {  // 32 warps: exclusive scan of the per-warp == T counts, totals
+    const int e = wb[lane], gtv = wb[32 + lane];
+    int incl = e, gsum = gtv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+      gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+    }
+    wb[64 + lane] = incl - e;
+    if (lane == 31) {
+      cnt[0] = gsum;
+      cnt[1] = incl;
+    }
+  }
+  cluster.sync();  // every CTA's totals are published
   if (tid < 32) {  // lane c reads CTA c's counts; sum over the lower ranks
     int gv = 0, ev = 0;
     if (lane < rank) {
@@ -285,22 +279,47 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
 
   if (p.top_k > 0) {
     const int gt_before = ctl[2], eq_before = ctl[3];
-    const int take_eq = max(0, min(krem - eq_before, cnt[1]));
-    const int sel_before = gt_before + min(eq_before, krem);
-    int eq_run = 0, sel_run = 0;
-    for (int it = 0; it < iters; ++it) {
-      const int j = it * blockDim.x + tid;
+    const int eq_rank0 = eq_before + wb[64 + wid];  // rank of this warp's first == T key
+    int sel_w = 0, eq_run = eq_rank0;
+    for (int i = 0; i < per; ++i) {
+      const int j = wbase + i * 32 + lane;
       const int pos = lo + j;
       const bool in = j < n_loc && pos >= c_lo && pos < c_hi;
       const uint32_t k = in ? (keys[j] & mask) : 0u;
-      const bool is_gt = in && k > T, is_eq = in && k == T;
-      int tot;
-      const int eq_rank = eq_run + block_excl_count(is_eq, wb, &tot);
-      eq_run += tot;
-      const bool sel = is_gt || (is_eq && eq_rank < take_eq);
-      const int slot = p.n_sink + sel_before + sel_run + block_excl_count(sel, wb, &tot);
-      sel_run += tot;
-      if (sel) out[slot] = pos;
+      const bool is_eq = in && k == T;
+      const unsigned eb = __ballot_sync(0xffffffffu, is_eq);
+      const bool sel = (in && k > T) || (is_eq && eq_run + __popc(eb & lt_mask) < krem);
+      sel_w += __popc(__ballot_sync(0xffffffffu, sel));
+      eq_run += __popc(eb);
+    }
+    if (lane == 0) wb[96 + wid] = sel_w;
+    __syncthreads();
+    if (wid == 0) {
+      const int v = wb[96 + lane];
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      wb[128 + lane] = incl - v;
+    }
+    __syncthreads();
+    const int slot0 = p.n_sink + gt_before + min(eq_before, krem) + wb[128 + wid];
+    int sel_run = 0;
+    eq_run = eq_rank0;
+    for (int i = 0; i < per; ++i) {
+      const int j = wbase + i * 32 + lane;
+      const int pos = lo + j;
+      const bool in = j < n_loc && pos >= c_lo && pos < c_hi;
+      const uint32_t k = in ? (keys[j] & mask) : 0u;
+      const bool is_eq = in && k == T;
+      const unsigned eb = __ballot_sync(0xffffffffu, is_eq);
+      const bool sel = (in && k > T) || (is_eq && eq_run + __popc(eb & lt_mask) < krem);
+      const unsigned sbal = __ballot_sync(0xffffffffu, sel);
+      if (sel) out[slot0 + sel_run + __popc(sbal & lt_mask)] = pos;
+      sel_run += __popc(sbal);
+      eq_run += __popc(eb);
     }
   }
   if (rank == 0) {
