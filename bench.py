@@ -119,8 +119,8 @@ def verify_traffic(workload):
         return None
     fields = {}
     for line in open(path):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
+        if ": " in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(": ", 1)
             fields[k.strip()] = v.strip()
     if fields.get("verify.cu sha256[:16]") != digest:
         return None
@@ -236,6 +236,66 @@ def run_reference(args, rank, world):
                               "d2h_bytes_per_step": 0}}))
 
 
+def run_stack(args, rank, world, local):
+    """The 32-layer decode loop: µs of attention kernels per draft/verify
+    iteration (k drafts x 32 layers, verify + select x 32 layers), summed from
+    CUDA events around every call.  Each layer's K/V (1.3 GB) is far larger
+    than L2, so every call starts cold without a flush."""
+    import dataclasses
+    import torch
+    from self_speculative_sparse_vg_gb300.stack import DecodeStack
+    from self_speculative_sparse_vg_gb300.workloads import STACKS
+    spec = dataclasses.replace(STACKS[args.workload], iterations=args.warmup + args.steps)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    st = DecodeStack(spec, dev)
+    st.seed_selection()
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    iters, nbytes = [], []
+    kv_row = spec.num_kv_heads * spec.head_dim * 2 * 2
+    R, k = spec.n_drafts + 1, spec.n_drafts
+    for _ in range(args.steps):
+        lens = st.lens.cpu().tolist()
+        st.timing = []
+        st.step()
+        torch.cuda.synchronize()
+        tot = {"verify": 0.0, "select": 0.0, "draft": 0.0}
+        for kind, a, b in st.timing:
+            tot[kind] += a.elapsed_time(b) * 1e3
+        iters.append(tot)
+        n_sel = [min(L, spec.n_sel_max) for L in lens]
+        per_layer = (sum((L + R) * kv_row + L * spec.num_kv_heads * 4 * 2 for L in lens) +
+                     sum(sum((n + t) * kv_row for n in n_sel) for t in range(1, k + 1)))
+        nbytes.append(per_layer * spec.layers)
+    st.timing = None
+    clocks = sampler.stop() if sampler else None
+    assert int(st.flag.item()) == 0, "device error flag set"
+    step_us = [sum(t.values()) for t in iters]
+    value = statistics.mean(step_us)
+    (value,) = reduce_max([value], world, dev)
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    gbs = statistics.mean(nbytes) / (value * 1e-6) / 1e9
+    print(json.dumps({
+        "metric": "us_per_decode_iteration_attention", "mode": "stack", "value": value,
+        "unit": "us", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see workloads.py)",
+        "config": {"workload": spec.name, "layers": spec.layers, "batch": spec.batch,
+                   "prefix_lens_at_start": list(spec.prefix_lens), "n_drafts": k,
+                   "top_k": spec.top_k, "n_sink": spec.n_sink, "n_recent": spec.n_recent,
+                   "l2": "no flush: each layer's K/V (1.3 GB) exceeds L2"},
+        "stages_us": {key: statistics.mean(t[key] for t in iters) for key in iters[0]},
+        "algorithmic_bytes_per_iteration": statistics.mean(nbytes),
+        "hbm_gbs": gbs, "hbm_frac": gbs / peak, "peak_kind": peak_kind,
+        "gpu_launches": args.steps * spec.layers * (2 * k + 3 + 1),
+        "clocks": clocks}))
+
+
 def _config(spec, n):
     return {"workload": spec.name, "batch": spec.batch, "num_q_heads": spec.num_q_heads,
             "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
@@ -268,7 +328,15 @@ def main():
     import torch.distributed as dist
     from self_speculative_sparse_vg_gb300 import vg
     from self_speculative_sparse_vg_gb300.step import DecodeStep
-    from self_speculative_sparse_vg_gb300.workloads import WORKLOADS, make_inputs
+    from self_speculative_sparse_vg_gb300.workloads import STACKS, WORKLOADS, make_inputs
+
+    if args.workload in STACKS:
+        if world > 1:
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        run_stack(args, rank, world, local)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)

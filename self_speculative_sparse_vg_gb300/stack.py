@@ -66,7 +66,10 @@ class DecodeStack:
     "verify" (tensors stay on the device).  force_selection(kind, layer), if
     given, is called once after each selection (after `record`); a returned
     (indices, counts) pair replaces the selection the next drafts use, so
-    that two decode loops can be run on one sequence of selections."""
+    that two decode loops can be run on one sequence of selections.
+    timing: if a list, every attention call appends (kind, start, end) CUDA
+    events recorded around it on the current stream ("verify", "select",
+    "draft")."""
 
     def __init__(self, spec: StackSpec, device="cuda", gen_device=None,
                  record: Optional[Callable] = None,
@@ -132,6 +135,7 @@ class DecodeStack:
         self.accepted: List[torch.Tensor] = []
         self.record = record
         self.force_selection = force_selection
+        self.timing: Optional[list] = None
 
     # ------------------------------------------------------------ pieces
     def _qkv(self, l, x):
@@ -154,15 +158,27 @@ class DecodeStack:
         self.kp[l][phys, :, slot] = k
         self.vp[l][phys, :, slot] = v
 
+    def _timed(self, kind, fn, *args, **kw):
+        if self.timing is None:
+            return fn(*args, **kw)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        r = fn(*args, **kw)
+        b.record()
+        self.timing.append((kind, a, b))
+        return r
+
     def _verify_select(self, l, q, R):
         s = self.spec
         out = torch.empty(s.batch, R, s.num_q_heads, s.head_dim, dtype=torch.bfloat16,
                           device=self.device)
-        vg.verify_attention(self.kv[l], q, self.lens, s.max_prefix, s.softmax_scale, out,
-                            vg.CAPTURE_GROUP_SUM, self.capture, 0, self.ws_verify[R], self.flag)
-        vg.select_kv(self.capture, vg.CAPTURE_GROUP_SUM, self.lens, s.num_q_heads,
-                     s.num_kv_heads, s.max_prefix, s.top_k, s.n_sink, s.n_recent, s.per_head,
-                     self.indices[l], self.counts[l], self.flag, workspace=self.ws_select)
+        self._timed("verify", vg.verify_attention, self.kv[l], q, self.lens, s.max_prefix,
+                    s.softmax_scale, out, vg.CAPTURE_GROUP_SUM, self.capture, 0,
+                    self.ws_verify[R], self.flag)
+        self._timed("select", vg.select_kv, self.capture, vg.CAPTURE_GROUP_SUM, self.lens,
+                    s.num_q_heads, s.num_kv_heads, s.max_prefix, s.top_k, s.n_sink, s.n_recent,
+                    s.per_head, self.indices[l], self.counts[l], self.flag,
+                    workspace=self.ws_select)
         return out
 
     def _forced(self, kind, l):
@@ -205,9 +221,9 @@ class DecodeStack:
                 self._write_kv(l, kk[:, None], vv[:, None], pos)
                 out = torch.empty(B, s.num_q_heads, s.head_dim, dtype=torch.bfloat16,
                                   device=self.device)
-                vg.sparse_draft_attention(self.kv[l], q, self.indices[l], self.counts[l],
-                                          s.per_head, self.tail_start, cur, self.max_tail,
-                                          s.softmax_scale, out, self.ws_draft, self.flag)
+                self._timed("draft", vg.sparse_draft_attention, self.kv[l], q, self.indices[l],
+                            self.counts[l], s.per_head, self.tail_start, cur, self.max_tail,
+                            s.softmax_scale, out, self.ws_draft, self.flag)
                 if self.record:
                     self.record("draft", l, dict(out=out, t=t))
                 x = x + out.double().reshape(B, -1)
