@@ -74,7 +74,17 @@ enum {
    * head][row k of each head][rows 1..k-1, head-major within a row]; each
    * block of 32 consecutive pairs is reduced by a fixed butterfly, and the
    * blocks' sums are added in ascending block order.                       */
-  VG_CAPTURE_ALL_SUM = 3
+  VG_CAPTURE_ALL_SUM = 3,
+  /* Every row, for attention-weight statistics (A Sparse Glimpse of the
+   * Whole, "What carries the argument": rank by the post-softmax weights of
+   * a window of verification queries; the window here is the n_rows block
+   * rows).  float32, two consecutive arrays:
+   *   logits [batch][num_q_heads][n_rows][max_prefix]: s[q][i][j] for the
+   *          prefix positions j < L_b (the rest untouched);
+   *   lse    [batch][num_q_heads][n_rows]: ln sum_{j <= L_b + i} exp(s[q][i][j]),
+   *          the row's softmax normaliser over everything it attends.
+   * Select on it with vg_select_kv_weights.                                */
+  VG_CAPTURE_ALL_ROWS = 4
 };
 
 /* Bits OR-ed into *error_flag by the kernels. */
@@ -174,6 +184,23 @@ vg_status vg_select_kv(const float* capture, int capture_mode, const int32_t* pr
                        int n_sink, int n_recent, int per_head, int32_t* indices, int32_t* counts,
                        int cap, void* workspace, size_t workspace_bytes, int32_t* error_flag,
                        cudaStream_t stream);
+
+/* Weight-statistics variant of vg_select_kv (A Sparse Glimpse of the Whole,
+ * "What carries the argument": rank positions by the attention weights of a
+ * window of verification queries instead of two raw logit rows).  `capture`
+ * is a VG_CAPTURE_ALL_ROWS capture of n_rows (<= 16) verify rows.  The score
+ * of prefix position j is
+ *   sum over the selection row's query heads q (ascending) and rows i
+ *   (ascending) of expf(logits[q][i][j] - lse[q][i]),
+ * i.e. the row-normalised post-softmax weights summed over the window (the
+ * mean ranks identically); float32, fixed order.  Everything else --
+ * candidates, sink/recent, ties, outputs, workspace, errors -- is as in
+ * vg_select_kv. */
+vg_status vg_select_kv_weights(const float* capture, int n_rows, const int32_t* prefix_lens,
+                               int batch, int num_q_heads, int num_kv_heads, int max_prefix,
+                               int top_k, int n_sink, int n_recent, int per_head,
+                               int32_t* indices, int32_t* counts, int cap, void* workspace,
+                               size_t workspace_bytes, int32_t* error_flag, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Sparse draft attention.

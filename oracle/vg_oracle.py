@@ -40,6 +40,7 @@ import numpy as np
 CAPTURE_GROUP_SUM = 1   # per-KV-head sum of the two captured rows
 CAPTURE_ROWS = 2        # the two raw rows per query head
 CAPTURE_ALL_SUM = 3     # per-KV-head sum of every verify row (Collect-All)
+CAPTURE_ALL_ROWS = 4    # every row's logits plus its softmax normaliser (weights)
 
 
 def _softmax_weights(s: np.ndarray) -> np.ndarray:
@@ -121,6 +122,52 @@ def collect_all_sum(q, k, prefix_lens, scale, num_kv_heads):
                     acc += scale * (kp @ q[b, i, qh])
             A[b, h, :L] = acc
     return A
+
+
+def capture_all_rows(q, k, prefix_lens, scale):
+    """Every verify row's logits and softmax normaliser, for weight
+    statistics.  [SSL] "What carries the argument" (the importance signal is
+    the attention weights of a window of verification queries; the window
+    here is the k+1 block rows).
+
+    Returns logits [B][Hq][R][Lmax] (scale*q.k at prefix positions j < L_b,
+    NaN beyond) and lse [B][Hq][R] = ln sum_{j <= L_b + i} exp(scale*q_i.k_j),
+    the normaliser of row i over everything it attends (R2)."""
+    B, R, Hq, d = q.shape
+    Hkv = k[0].shape[0]
+    g = Hq // Hkv
+    Lmax = int(max(prefix_lens))
+    logits = np.full((B, Hq, R, Lmax), np.nan)
+    lse = np.zeros((B, Hq, R))
+    for b in range(B):
+        L = int(prefix_lens[b])
+        for h in range(Hq):
+            for i in range(R):
+                s = scale * (k[b][h // g, :L + i + 1] @ q[b, i, h])
+                logits[b, h, i, :L] = s[:L]
+                m = s.max()
+                lse[b, h, i] = m + np.log(np.exp(s - m).sum())
+    return logits, lse
+
+
+def weight_scores(logits, lse, num_kv_heads, per_head):
+    """Selection score from post-softmax weights: for each prefix position,
+    the sum over the selection row's query heads and all window rows of
+    exp(logit - lse).  [SSL] "What carries the argument"; a sum ranks like
+    the mean.  Returns [B][1 or Hkv][Lmax] float64."""
+    B, Hq, R, Lmax = logits.shape
+    g = Hq // num_kv_heads
+    w = np.exp(logits - lse[..., None])              # [B][Hq][R][Lmax]
+    per_q = w.sum(axis=2)                            # [B][Hq][Lmax]
+    G = per_q.reshape(B, num_kv_heads, g, Lmax).sum(axis=2)
+    return G if per_head else G.sum(axis=1, keepdims=True)
+
+
+def select_kv_weights(logits, lse, prefix_lens, num_kv_heads, top_k, n_sink, n_recent, per_head):
+    """Index sets from weight_scores, by select_row."""
+    sc = weight_scores(logits, lse, num_kv_heads, per_head)
+    return [[select_row(sc[b, r], L, top_k, n_sink, n_recent) for r in range(sc.shape[1])]
+            for b, L in enumerate(prefix_lens)]
 
 
 def group_sum(rows, num_kv_heads):

@@ -43,6 +43,8 @@ struct SelectParams {
   int32_t* error_flag;
   int capture_mode, batch, num_q_heads, num_kv_heads, group, max_prefix;
   int top_k, n_sink, n_recent, per_head, cap, rows, slice;
+  int n_rows;         // VG_CAPTURE_ALL_ROWS: verify rows per head
+  size_t lse_offset;  // VG_CAPTURE_ALL_ROWS: floats before the per-row normalisers
 };
 
 // Order-preserving map float -> uint32 (larger float -> larger key), -0 as +0.
@@ -60,6 +62,35 @@ constexpr int kLoadBatch = 16;
 
 __device__ __forceinline__ float row_score(const SelectParams& p, int b, int row, int j) {
   const size_t L = p.max_prefix;
+  if (p.capture_mode == VG_CAPTURE_ALL_ROWS) {
+    // sum of post-softmax weights exp(s - lse) over the rows and query heads
+    // of the selection row, in the order (KV head, query head, verify row)
+    const int g = p.group, R = p.n_rows;
+    const int h0 = p.per_head ? row : 0, h1 = p.per_head ? row + 1 : p.num_kv_heads;
+    float acc = 0.f;
+    bool first = true;
+    for (int q = h0 * g; q < h1 * g; ++q) {
+      const size_t base = ((size_t)b * p.num_q_heads + q) * R;
+      for (int i0 = 0; i0 < R; i0 += kLoadBatch) {
+        float s[kLoadBatch], z[kLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {  // every load of the batch before any use
+          const bool ok = i0 + u < R;
+          s[u] = ok ? __ldg(p.capture + (base + i0 + u) * L + j) : 0.f;
+          z[u] = ok ? __ldg(p.capture + p.lse_offset + base + i0 + u) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+          if (i0 + u < R) {
+            const float w = expf(s[u] - z[u]);
+            acc = first ? w : acc + w;
+            first = false;
+          }
+        }
+      }
+    }
+    return acc;
+  }
   if (p.capture_mode == VG_CAPTURE_GROUP_SUM) {
     const float* G = p.capture + (size_t)b * p.num_kv_heads * L + j;
     if (p.per_head) return __ldg(G + (size_t)row * L);
@@ -353,17 +384,48 @@ extern "C" size_t vg_select_workspace_bytes(int batch, int num_kv_heads, int max
   return align_up((size_t)batch * rows * max_prefix * 4, 256);
 }
 
+static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
+                             const int32_t* prefix_lens, int batch, int num_q_heads,
+                             int num_kv_heads, int max_prefix, int top_k, int n_sink,
+                             int n_recent, int per_head, int32_t* indices, int32_t* counts,
+                             int cap, void* workspace, size_t workspace_bytes,
+                             int32_t* error_flag, cudaStream_t stream);
+
 extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
                                   const int32_t* prefix_lens, int batch, int num_q_heads,
                                   int num_kv_heads, int max_prefix, int top_k, int n_sink,
                                   int n_recent, int per_head, int32_t* indices, int32_t* counts,
                                   int cap, void* workspace, size_t workspace_bytes,
                                   int32_t* error_flag, cudaStream_t stream) {
-  if (!capture || !prefix_lens || !indices || !counts || batch <= 0 || num_q_heads <= 0 ||
-      num_kv_heads <= 0 || max_prefix <= 0 || top_k < 0 || n_sink < 0 || n_recent < 0 || cap <= 0)
-    return VG_ERR_INVALID_ARGUMENT;
   if (capture_mode == VG_CAPTURE_ALL_SUM) capture_mode = VG_CAPTURE_GROUP_SUM;  // same layout
   if (capture_mode != VG_CAPTURE_GROUP_SUM && capture_mode != VG_CAPTURE_ROWS)
+    return VG_ERR_INVALID_ARGUMENT;
+  return select_impl(capture, capture_mode, 0, prefix_lens, batch, num_q_heads, num_kv_heads,
+                     max_prefix, top_k, n_sink, n_recent, per_head, indices, counts, cap,
+                     workspace, workspace_bytes, error_flag, stream);
+}
+
+extern "C" vg_status vg_select_kv_weights(const float* capture, int n_rows,
+                                          const int32_t* prefix_lens, int batch, int num_q_heads,
+                                          int num_kv_heads, int max_prefix, int top_k, int n_sink,
+                                          int n_recent, int per_head, int32_t* indices,
+                                          int32_t* counts, int cap, void* workspace,
+                                          size_t workspace_bytes, int32_t* error_flag,
+                                          cudaStream_t stream) {
+  if (n_rows <= 0 || n_rows > 16) return VG_ERR_INVALID_ARGUMENT;
+  return select_impl(capture, VG_CAPTURE_ALL_ROWS, n_rows, prefix_lens, batch, num_q_heads,
+                     num_kv_heads, max_prefix, top_k, n_sink, n_recent, per_head, indices, counts,
+                     cap, workspace, workspace_bytes, error_flag, stream);
+}
+
+static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
+                             const int32_t* prefix_lens, int batch, int num_q_heads,
+                             int num_kv_heads, int max_prefix, int top_k, int n_sink,
+                             int n_recent, int per_head, int32_t* indices, int32_t* counts,
+                             int cap, void* workspace, size_t workspace_bytes,
+                             int32_t* error_flag, cudaStream_t stream) {
+  if (!capture || !prefix_lens || !indices || !counts || batch <= 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || max_prefix <= 0 || top_k < 0 || n_sink < 0 || n_recent < 0 || cap <= 0)
     return VG_ERR_INVALID_ARGUMENT;
   if (num_q_heads % num_kv_heads) return VG_ERR_INVALID_ARGUMENT;
   if (num_q_heads / num_kv_heads > 8) return VG_ERR_UNSUPPORTED;
@@ -382,6 +444,8 @@ extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
   p.counts = counts;
   p.error_flag = error_flag;
   p.capture_mode = capture_mode;
+  p.n_rows = n_rows;
+  p.lse_offset = (size_t)batch * num_q_heads * (n_rows > 0 ? n_rows : 1) * max_prefix;
   p.batch = batch;
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = num_kv_heads;

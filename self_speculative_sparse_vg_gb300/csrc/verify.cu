@@ -55,6 +55,7 @@ struct VerifyParams {
   int batch, n_rows, num_q_heads, num_kv_heads, group, m_rows, m_tiles;
   int max_prefix, max_pages_per_seq, num_pages;
   int capture_mode, splits, tiles_per_split, stages, groups;
+  size_t lse_offset;  // VG_CAPTURE_ALL_ROWS: floats before the per-row normalisers
   float scale, scale_log2;
 };
 
@@ -123,7 +124,7 @@ struct VerifyBars {
 
 // Softmax warp of a copy; COLS = 128 / CS columns of each tile, handled in
 // chunks of 32 (two passes over TMEM when COLS > 32: maximum, then P).
-template <int HD, int COLS>
+template <int HD, int COLS, int CM>
 __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const VerifyBars& bars,
                                                uint8_t* ring, float* cap_s, float* all_s,
                                                uint32_t tmem, int b, int h, int split, int t0,
@@ -144,9 +145,10 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
     lim = L + ri;
   }
   const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
-  const bool cap_two = wq == 0 && (p.capture_mode == VG_CAPTURE_GROUP_SUM ||
-                                   p.capture_mode == VG_CAPTURE_ROWS);
-  const bool cap_all = p.capture_mode == VG_CAPTURE_ALL_SUM;
+  // capture mode CM is a template parameter: each mode is its own kernel
+  const bool cap_two = wq == 0 && (CM == VG_CAPTURE_GROUP_SUM || CM == VG_CAPTURE_ROWS);
+  constexpr bool cap_all = CM == VG_CAPTURE_ALL_SUM;
+  constexpr bool cap_rows = CM == VG_CAPTURE_ALL_ROWS;
   const int s1 = (R > 1) ? g : 0;           // packed row of "row k, head 0"
   const int nrows = (R > 1) ? 2 * g : g;    // captured rows
   float* cap_w = cap_s + warp * 16 * kCapStride;
@@ -172,6 +174,20 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
       tmem_ld32(sbuf + col0 + k * kChunk, s);
       const int kpos = cpos + k * kChunk;
       if (kpos < L) {
+        if (cap_rows && m < M) {  // every row, raw, for weight statistics
+          float* dst = p.capture + (((size_t)b * p.num_q_heads + h * g + rq) * R + ri) * p.max_prefix + kpos;
+          const int nj = min(kChunk, L - kpos);
+          if (nj == kChunk && (p.max_prefix & 3) == 0) {
+#pragma unroll
+            for (int j = 0; j < kChunk; j += 4)
+              *reinterpret_cast<float4*>(dst + j) =
+                  make_float4(s[j] * p.scale, s[j + 1] * p.scale, s[j + 2] * p.scale, s[j + 3] * p.scale);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j)
+              if (j < nj) dst[j] = s[j] * p.scale;
+          }
+        }
         if (cap_two) {
           if (lane < nrows) {
 #pragma unroll
@@ -179,7 +195,7 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
           }
           __syncwarp();
           if (kpos + lane < L) {
-            if (p.capture_mode == VG_CAPTURE_GROUP_SUM) {
+            if (CM == VG_CAPTURE_GROUP_SUM) {
               float G = cap_w[lane] + cap_w[s1 * kCapStride + lane];
               for (int qi = 1; qi < g; ++qi)
                 G = G + (cap_w[qi * kCapStride + lane] + cap_w[(s1 + qi) * kCapStride + lane]);
@@ -391,9 +407,12 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
     ml[0] = mxr;
     ml[1] = lt_all;
   }
+  if (m < M && p.splits == 1 && cap_rows)  // the row's normaliser: (m + log2 l) ln 2
+    p.capture[p.lse_offset + ((size_t)b * p.num_q_heads + h * g + rq) * R + ri] =
+        (mxr + __log2f(lt_all)) * 0.6931471805599453f;
 }
 
-template <int HD>
+template <int HD, int CM>
 __global__ void __launch_bounds__(kVerifyThreads, 1)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const VerifyParams p) {
@@ -618,11 +637,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   } else if (warp < NAW) {
     // ---------------------------------------------------------- softmax
     if (CS == 4)
-      verify_softmax<HD, 32>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
+      verify_softmax<HD, 32, CM>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
     else if (CS == 2)
-      verify_softmax<HD, 64>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
+      verify_softmax<HD, 64, CM>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
     else
-      verify_softmax<HD, 128>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
+      verify_softmax<HD, 128, CM>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
   }
   tc_fence_before();
   __syncthreads();  // every TMEM access and every MMA of this CTA is done
@@ -653,7 +672,11 @@ __global__ void __launch_bounds__(kMergeThreads) verify_merge_kernel(const Verif
   row_of(m, p.group, p.n_rows, i, qi);
   merge_splits<HD>(p.part_o + (bh * S * M + m) * HD, (size_t)M * HD, p.part_ml + (bh * S * M + m) * 2,
                    (size_t)M * 2, S,
-                   p.out + ((size_t)(b * p.n_rows + i) * p.num_q_heads + h * p.group + qi) * HD, smem_f);
+                   p.out + ((size_t)(b * p.n_rows + i) * p.num_q_heads + h * p.group + qi) * HD, smem_f,
+                   p.capture_mode == VG_CAPTURE_ALL_ROWS
+                       ? p.capture + p.lse_offset +
+                             ((size_t)b * p.num_q_heads + h * p.group + qi) * p.n_rows + i
+                       : nullptr);
 }
 
 struct VerifyPlan {
@@ -700,14 +723,14 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   return true;
 }
 
-template <int HD>
-cudaError_t launch_verify(const VerifyPlan& pl, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const VerifyParams& p, dim3 grid, cudaStream_t stream) {
+template <int HD, int CM>
+cudaError_t launch_verify_main(const VerifyPlan& pl, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const VerifyParams& p, dim3 grid, cudaStream_t stream) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<HD>,
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<HD, CM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -722,7 +745,20 @@ cudaError_t launch_verify(const VerifyPlan& pl, const CUtensorMap& tk, const CUt
   vcfg.stream = stream;
   vcfg.attrs = pdl;
   vcfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&vcfg, verify_kernel<HD>, tk, tv, p);
+  return cudaLaunchKernelEx(&vcfg, verify_kernel<HD, CM>, tk, tv, p);
+}
+
+template <int HD>
+cudaError_t launch_verify(const VerifyPlan& pl, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const VerifyParams& p, dim3 grid, cudaStream_t stream) {
+  cudaError_t e;
+  switch (p.capture_mode) {
+    case VG_CAPTURE_GROUP_SUM: e = launch_verify_main<HD, VG_CAPTURE_GROUP_SUM>(pl, tk, tv, p, grid, stream); break;
+    case VG_CAPTURE_ROWS: e = launch_verify_main<HD, VG_CAPTURE_ROWS>(pl, tk, tv, p, grid, stream); break;
+    case VG_CAPTURE_ALL_SUM: e = launch_verify_main<HD, VG_CAPTURE_ALL_SUM>(pl, tk, tv, p, grid, stream); break;
+    case VG_CAPTURE_ALL_ROWS: e = launch_verify_main<HD, VG_CAPTURE_ALL_ROWS>(pl, tk, tv, p, grid, stream); break;
+    default: e = launch_verify_main<HD, VG_CAPTURE_NONE>(pl, tk, tv, p, grid, stream); break;
+  }
   if (e != cudaSuccess || pl.splits == 1) return e;
   // split merge, chained with programmatic dependent launch
   cudaLaunchConfig_t cfg = {};
@@ -765,7 +801,8 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
       max_prefix <= 0 || num_splits < 0 || !(softmax_scale == softmax_scale))
     return VG_ERR_INVALID_ARGUMENT;
   if (capture_mode != VG_CAPTURE_NONE && capture_mode != VG_CAPTURE_GROUP_SUM &&
-      capture_mode != VG_CAPTURE_ROWS && capture_mode != VG_CAPTURE_ALL_SUM)
+      capture_mode != VG_CAPTURE_ROWS && capture_mode != VG_CAPTURE_ALL_SUM &&
+      capture_mode != VG_CAPTURE_ALL_ROWS)
     return VG_ERR_INVALID_ARGUMENT;
   if (capture_mode != VG_CAPTURE_NONE && !capture) return VG_ERR_INVALID_ARGUMENT;
   if (num_q_heads % kv->num_kv_heads) return VG_ERR_INVALID_ARGUMENT;
@@ -806,6 +843,7 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
   p.max_pages_per_seq = kv->max_pages_per_seq;
   p.num_pages = kv->num_pages;
   p.capture_mode = capture_mode;
+  p.lse_offset = (size_t)batch * num_q_heads * n_rows * max_prefix;
   p.splits = pl.splits;
   p.tiles_per_split = pl.tiles_per_split;
   p.stages = pl.stages;

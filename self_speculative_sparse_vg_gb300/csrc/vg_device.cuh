@@ -346,7 +346,8 @@ constexpr int kMergeSmemFloats = 8 + 128 + 4 * kMergeThreads;
 template <int HD>
 __device__ __forceinline__ void merge_splits(const float* o_base, size_t o_stride,
                                              const float* ml_base, size_t ml_stride, int S,
-                                             __nv_bfloat16* dst, float* smem_f) {
+                                             __nv_bfloat16* dst, float* smem_f,
+                                             float* lse = nullptr) {
   constexpr int COLS = HD / 4;
   constexpr int G = kMergeThreads / COLS;
   const int t = threadIdx.x, col = t % COLS, grp = t / COLS;
@@ -426,6 +427,8 @@ __device__ __forceinline__ void merge_splits(const float* o_base, size_t o_strid
     *reinterpret_cast<__nv_bfloat162*>(dst + col * 4) = __floats2bfloat162_rn(o.x * inv, o.y * inv);
     *reinterpret_cast<__nv_bfloat162*>(dst + col * 4 + 2) =
         __floats2bfloat162_rn(o.z * inv, o.w * inv);
+    // natural-log sum of the row's exponentials: (m + log2 l) ln 2
+    if (lse && col == 0) *lse = (mx_all + __log2f(lt_all)) * 0.6931471805599453f;
   }
 }
 

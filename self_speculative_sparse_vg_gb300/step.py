@@ -48,6 +48,9 @@ class DecodeStep:
         kv = vg.PagedKV(inp.k_pages.to(dev), inp.v_pages.to(dev), inp.page_table.to(dev))
         if capture_mode == vg.CAPTURE_ROWS:
             capture = torch.zeros(B, Hq, 2, Lmax, dtype=torch.float32, device=dev)
+        elif capture_mode == vg.CAPTURE_ALL_ROWS:
+            capture = torch.zeros(vg.all_rows_capture_floats(B, Hq, R, Lmax), dtype=torch.float32,
+                                  device=dev)
         else:
             capture = torch.zeros(B, Hkv, Lmax, dtype=torch.float32, device=dev)
         rows = Hkv if per_head else 1
@@ -90,6 +93,11 @@ class DecodeStep:
                  sp.max_prefix, ctypes.c_float(sp.softmax_scale), p(self.out_verify),
                  self.capture_mode, p(self.capture), self.num_splits, p(self.ws_verify),
                  self.ws_verify.numel(), p(self.error_flag), st)
+        elif kind == "select" and self.capture_mode == vg.CAPTURE_ALL_ROWS:
+            a = (p(self.capture), R, p(self.prefix_lens), B, Hq, sp.num_kv_heads,
+                 sp.max_prefix, sp.top_k, sp.n_sink, sp.n_recent, int(self.per_head),
+                 p(self.indices), p(self.counts), self.indices.shape[-1], p(self.ws_select),
+                 self.ws_select.numel(), p(self.error_flag), st)
         elif kind == "select":
             a = (p(self.capture), self.capture_mode, p(self.prefix_lens), B, Hq, sp.num_kv_heads,
                  sp.max_prefix, sp.top_k, sp.n_sink, sp.n_recent, int(self.per_head),
@@ -108,7 +116,11 @@ class DecodeStep:
         vg._check("vg_verify_attention", vg._lib.vg_verify_attention(*self._args("verify", 0, stream)))
 
     def select(self, stream=None):
-        vg._check("vg_select_kv", vg._lib.vg_select_kv(*self._args("select", 0, stream)))
+        if self.capture_mode == vg.CAPTURE_ALL_ROWS:
+            vg._check("vg_select_kv_weights",
+                      vg._lib.vg_select_kv_weights(*self._args("select", 0, stream)))
+        else:
+            vg._check("vg_select_kv", vg._lib.vg_select_kv(*self._args("select", 0, stream)))
 
     def draft(self, t: int, stream=None):
         """Draft step t = 1..k: query at position L + t - 1, tail [L, L + t)."""

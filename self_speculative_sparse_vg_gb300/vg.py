@@ -19,6 +19,7 @@ CAPTURE_NONE = 0
 CAPTURE_GROUP_SUM = 1
 CAPTURE_ROWS = 2
 CAPTURE_ALL_SUM = 3
+CAPTURE_ALL_ROWS = 4
 
 DEVERR_PAGE = 1
 DEVERR_INDEX = 2
@@ -28,7 +29,7 @@ DEVERR_LENGTH = 16
 
 EXPORTED = (
     "vg_verify_workspace_bytes", "vg_verify_attention",
-    "vg_select_workspace_bytes", "vg_select_kv",
+    "vg_select_workspace_bytes", "vg_select_kv", "vg_select_kv_weights",
     "vg_sparse_draft_workspace_bytes", "vg_sparse_draft_attention",
     "vg_status_string", "vg_version",
     "vg_verify_noalloc_scratch_bytes", "vg_verify_attention_noalloc",
@@ -60,6 +61,8 @@ def _load():
         "vg_verify_attention": (i32, [kvp, vp, vp, i32, i32, i32, i32, f32, vp, i32, vp, i32,
                                       vp, sz, vp, vp]),
         "vg_select_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "vg_select_kv_weights": (i32, [vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp,
+                                       vp, i32, vp, sz, vp, vp]),
         "vg_select_kv": (i32, [vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, i32,
                                vp, sz, vp, vp]),
         "vg_sparse_draft_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
@@ -189,6 +192,30 @@ def select_kv(capture, capture_mode, prefix_lens, num_q_heads, num_kv_heads, max
                           int(bool(per_head)), _ptr(indices), _ptr(counts), cap, _ptr(workspace),
                           workspace.numel(), _ptr(error_flag), _stream(stream))
     _check("vg_select_kv", s)
+    return indices, counts
+
+
+def all_rows_capture_floats(batch, num_q_heads, n_rows, max_prefix) -> int:
+    """Float count of a VG_CAPTURE_ALL_ROWS capture: logits, then row lse."""
+    return batch * num_q_heads * n_rows * (max_prefix + 1)
+
+
+def select_kv_weights(capture, n_rows, prefix_lens, num_q_heads, num_kv_heads, max_prefix,
+                      top_k, n_sink, n_recent, per_head, indices, counts, error_flag=None,
+                      stream=None, workspace=None):
+    """vg_select_kv_weights: selection by the post-softmax weights of the
+    n_rows captured rows (capture from VG_CAPTURE_ALL_ROWS)."""
+    B = prefix_lens.shape[0]
+    cap = indices.shape[-1]
+    if workspace is None:
+        workspace = zero_workspace(select_workspace_bytes(B, num_kv_heads, max_prefix, per_head),
+                                   indices.device)
+    s = _lib.vg_select_kv_weights(_ptr(capture), int(n_rows), _ptr(prefix_lens), B, num_q_heads,
+                                  num_kv_heads, int(max_prefix), int(top_k), int(n_sink),
+                                  int(n_recent), int(bool(per_head)), _ptr(indices), _ptr(counts),
+                                  cap, _ptr(workspace), workspace.numel(), _ptr(error_flag),
+                                  _stream(stream))
+    _check("vg_select_kv_weights", s)
     return indices, counts
 
 

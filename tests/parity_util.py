@@ -72,9 +72,31 @@ def oracle_all(inp):
     return O.collect_all_sum(q, k, s.prefix_lens, s.softmax_scale, s.num_kv_heads)
 
 
+GAP_W_REL = 1e-3  # weight scores: near-tie allowance relative to the k-th score
+
+
+def oracle_weights(inp):
+    """VG_CAPTURE_ALL_ROWS of the oracle: (logits [B][Hq][R][Lmax], lse [B][Hq][R])."""
+    q, k, _ = dense64(inp)
+    return O.capture_all_rows(q, k, inp.spec.prefix_lens, inp.spec.softmax_scale)
+
+
+def split_all_rows(flat, spec):
+    B, Hq, R, Lmax = spec.batch, spec.num_q_heads, spec.n_rows, spec.max_prefix
+    a = np.asarray(flat)
+    return a[:B * Hq * R * Lmax].reshape(B, Hq, R, Lmax), a[B * Hq * R * Lmax:].reshape(B, Hq, R)
+
+
 def check_capture(st, inp, rows64):
     s = inp.spec
     cap = st.capture.cpu().numpy()
+    if st.capture_mode == O.CAPTURE_ALL_ROWS:
+        lg, ls = split_all_rows(cap, s)
+        olg, ols = oracle_weights(inp)
+        for b, L in enumerate(s.prefix_lens):
+            assert_close_capture(lg[b, :, :, :L], olg[b, :, :, :L], f"all-rows logits b={b}")
+            assert_close_capture(ls[b], ols[b], f"row lse b={b}")
+        return
     if st.capture_mode == O.CAPTURE_ALL_SUM:
         A = oracle_all(inp)
         for b, L in enumerate(s.prefix_lens):
@@ -126,6 +148,15 @@ def check_select_synthetic(spec, capture_mode, per_head, seed=5, device="cuda"):
             assert (got_i[b, r, n:] == -1).all(), "padding must be -1"
 
 
+def _weight_sets_scores(inp, per_head):
+    s = inp.spec
+    olg, ols = oracle_weights(inp)
+    sc = O.weight_scores(olg, ols, s.num_kv_heads, per_head)
+    sets = O.select_kv_weights(olg, ols, s.prefix_lens, s.num_kv_heads, s.top_k, s.n_sink,
+                               s.n_recent, per_head)
+    return sets, sc
+
+
 def _oracle_capture(inp, rows64, capture_mode):
     """The oracle's capture for a capture mode: Collect-All sums, or the raw
     rows (from which the Collect-2 group sums follow)."""
@@ -136,6 +167,8 @@ def _oracle_capture(inp, rows64, capture_mode):
 
 def oracle_sets(inp, rows64, per_head, capture_mode=O.CAPTURE_GROUP_SUM):
     s = inp.spec
+    if capture_mode == O.CAPTURE_ALL_ROWS:
+        return _weight_sets_scores(inp, per_head)[0]
     cap, mode = _oracle_capture(inp, rows64, capture_mode)
     return O.select_kv(cap, mode, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
                        s.top_k, s.n_sink, s.n_recent, per_head)
@@ -144,10 +177,15 @@ def oracle_sets(inp, rows64, per_head, capture_mode=O.CAPTURE_GROUP_SUM):
 def check_select_end_to_end(st, inp, rows64):
     """GPU capture -> GPU select vs float64 oracle capture -> float64 select."""
     s = inp.spec
-    cap, mode = _oracle_capture(inp, rows64, st.capture_mode)
-    sc = O.selection_scores(cap, mode, s.num_q_heads, s.num_kv_heads, st.per_head)
-    ref = O.select_kv(cap, mode, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
-                      s.top_k, s.n_sink, s.n_recent, st.per_head)
+    gap_rel = False
+    if st.capture_mode == O.CAPTURE_ALL_ROWS:
+        ref, sc = _weight_sets_scores(inp, st.per_head)
+        gap_rel = True
+    else:
+        cap, mode = _oracle_capture(inp, rows64, st.capture_mode)
+        sc = O.selection_scores(cap, mode, s.num_q_heads, s.num_kv_heads, st.per_head)
+        ref = O.select_kv(cap, mode, s.prefix_lens, s.num_q_heads, s.num_kv_heads,
+                          s.top_k, s.n_sink, s.n_recent, st.per_head)
     got = gpu_sets(st)
     worst = 0.0
     for b, L in enumerate(s.prefix_lens):
@@ -161,7 +199,8 @@ def check_select_end_to_end(st, inp, rows64):
             for pos in a ^ o:
                 gap = abs(sc[b, r, pos] - kth)
                 worst = max(worst, gap)
-                assert gap < GAP, f"b={b} row={r} pos={pos}: score gap {gap:.3e} to the k-th"
+                lim = GAP_W_REL * abs(kth) if gap_rel else GAP
+                assert gap < lim, f"b={b} row={r} pos={pos}: score gap {gap:.3e} to the k-th"
     return worst
 
 

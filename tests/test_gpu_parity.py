@@ -79,6 +79,36 @@ def test_small_step_collect_all(name, per_head):
     P.check_drafts(st, inp, P.oracle_sets(inp, rows64, per_head, capture_mode=3))
 
 
+@pytest.mark.parametrize("name", ["base", "d64", "g8", "g5", "k0", "short", "m96"])
+@pytest.mark.parametrize("per_head", [False, True])
+def test_small_step_attention_weights(name, per_head):
+    """All-rows capture (every row's logits and softmax normaliser) and the
+    selection by summed post-softmax weights, against the oracle."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    spec = small_spec(**{**SMALL, **SMALL_EXTRA}[name])
+    inp, st = _run(spec, capture_mode=4, per_head=per_head)
+    P.check_verify(st, inp)
+    P.check_capture(st, inp, None)
+    P.check_select_end_to_end(st, inp, None)
+    P.check_drafts(st, inp, P.oracle_sets(inp, None, per_head, capture_mode=4))
+
+
+def test_attention_weights_split_invariance():
+    """The row normaliser written by the split merge equals the one written
+    by a single split, within float32 rounding."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    spec = small_spec(prefix_lens=(3000, 1777))
+    lses = []
+    for ns in (1, 7, 20):
+        inp, st = _run(spec, capture_mode=4, num_splits=ns)
+        P.check_capture(st, inp, None)
+        lses.append(P.split_all_rows(st.capture.cpu().numpy(), spec)[1])
+    for x in lses[1:]:
+        np.testing.assert_allclose(x, lses[0], rtol=1e-5, atol=1e-5)
+
+
 def test_ties_select_lower_position():
     """All-equal captured scores: the kept candidates are the lowest positions."""
     _require_gpu()

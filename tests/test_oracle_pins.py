@@ -358,3 +358,53 @@ def test_collect_all_hand_values():
     A = O.collect_all_sum(q, k, [3], 2.0, 1)
     total = 1 + 2 + 0.5 - 1 + 4 + 0.25
     np.testing.assert_array_equal(A[0, 0], 2.0 * total * np.array([1.0, -2.0, 3.0]))
+
+
+def test_all_rows_lse_is_logsumexp_of_the_causal_score_matrix():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(51)
+    q, k, _ = _rand_case(rng, 2, 4, 6, 3, 8, [21, 9])
+    logits, lse = O.capture_all_rows(q, k, [21, 9], 0.35)
+    for b, L in enumerate([21, 9]):
+        Hkv = k[b].shape[0]
+        K = np.repeat(k[b], 6 // Hkv, axis=0)          # repeat-KV GQA expansion
+        for h in range(6):
+            S = 0.35 * q[b, :, h, :] @ K[h].T           # [R][L + R], textbook full scores
+            for i in range(4):
+                np.testing.assert_allclose(lse[b, h, i], logsumexp(S[i, :L + i + 1]), rtol=1e-12)
+                np.testing.assert_allclose(logits[b, h, i, :L], S[i, :L], rtol=0, atol=1e-12)
+
+
+def test_weight_scores_are_row_normalised_weights():
+    """Each row's weights over everything it attends sum to 1, so the prefix
+    part plus the (separately computed) block part of the per-head sums is
+    exactly the number of window rows; constant keys give 1 / (L + i + 1)."""
+    rng = np.random.default_rng(52)
+    q, k, _ = _rand_case(rng, 1, 3, 4, 2, 8, [30])
+    logits, lse = O.capture_all_rows(q, k, [30], 0.5)
+    sc = O.weight_scores(logits, lse, 2, True)           # [1][2][30]
+    for h in range(2):
+        block = 0.0
+        for qh in (2 * h, 2 * h + 1):
+            for i in range(3):
+                s_blk = 0.5 * (k[0][h, 30:30 + i + 1] @ q[0, i, qh])
+                block += np.exp(s_blk - lse[0, qh, i]).sum()
+        np.testing.assert_allclose(sc[0, h].sum() + block, 2 * 3, rtol=1e-12)
+    kc = [np.ones((2, 33, 8))]
+    logits, lse = O.capture_all_rows(q, kc, [30], 0.5)
+    sc = O.weight_scores(logits, lse, 2, False)
+    want = 4 * sum(1.0 / (30 + i + 1) for i in range(3))
+    np.testing.assert_allclose(sc[0, 0], want, rtol=1e-12)
+
+
+def test_weight_selection_ranks_like_logits_for_one_row_and_head():
+    """With one query head and one row, exp(s - lse) is increasing in s, so
+    the weight-ranked selection equals the logit-ranked one."""
+    rng = np.random.default_rng(53)
+    q, k, _ = _rand_case(rng, 2, 1, 1, 1, 16, [200, 77])
+    logits, lse = O.capture_all_rows(q, k, [200, 77], 0.25)
+    a = O.select_kv_weights(logits, lse, [200, 77], 1, 20, 2, 5, False)
+    rows = O.capture_rows(q, k, [200, 77], 0.25)
+    b_ = O.select_kv(rows, O.CAPTURE_ROWS, [200, 77], 1, 1, 20, 2, 5, False)
+    for x, y in zip(a, b_):
+        assert x[0].tolist() == y[0].tolist()
