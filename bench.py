@@ -510,6 +510,45 @@ def main():
             tot += len(s2)
     capture_study["selection_overlap_collect2_vs_all"] = inter / max(tot, 1)
     del cap_rows, cap_all, ws1
+
+    # ---------------- sparse verification (merged schedule): each row keeps
+    # 7 % of the prefix blocks, rows sharing three quarters of them
+    from self_speculative_sparse_vg_gb300.workloads import make_block_selection
+    blocks, counts = make_block_selection(spec, 0.07, 11)
+    bl_d, ct_d = blocks.to(dev), counts.to(dev)
+    out_sv = torch.empty(st.q_verify.shape, dtype=torch.bfloat16, device=dev)
+    ws_sv = vg.zero_workspace(vg.sparse_verify_workspace_bytes(
+        B_, R_, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.max_prefix,
+        blocks.shape[-1]), dev)
+    sv_t = []
+    for i in range(33):
+        flush(i)
+        a, b_ = ev(), ev()
+        a.record(stream)
+        vg.sparse_verify_attention(st.kv, st.q_verify, st.prefix_lens, spec.max_prefix,
+                                   spec.softmax_scale, bl_d, ct_d, out_sv, workspace=ws_sv,
+                                   error_flag=st.error_flag)
+        b_.record(stream)
+        if i >= 3:
+            sv_t.append((a, b_))
+    torch.cuda.synchronize()
+    union = rows_sum = 0
+    for b_i, L in enumerate(spec.prefix_lens):
+        tail = set(range(L // 16, (L + R_ + 15) // 16))
+        u = set(tail)
+        for i in range(R_):
+            sel = set(blocks[b_i, i, :int(counts[b_i, i])].tolist())
+            u |= sel
+            rows_sum += len(sel | tail)
+        union += len(u)
+    page_bytes = spec.num_kv_heads * 16 * spec.head_dim * 2 * 2
+    sparse_study = {
+        "sparse_verify_us": statistics.median(x.elapsed_time(y) * 1e3 for x, y in sv_t),
+        "dense_verify_us": capture_study["verify_us_no_capture"],
+        "row_block_fraction": 0.07, "union_pages": union, "row_pages_summed": rows_sum,
+        "pages_loaded_per_row_page": union / max(rows_sum, 1),
+        "union_bytes": union * page_bytes}
+    del ws_sv, out_sv
     assert int(st.error_flag.item()) == 0, "device error flag set"
 
     value, e2e_val, hot_val = reduce_max([local_val, e2e_us, hot_us], world, dev)
@@ -543,6 +582,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * st.launches_per_step(),
         "capture_rules": capture_study,
+        "sparse_verification": sparse_study,
         "projection": speedup_projection(0.7, k, statistics.mean(dra) / max(k, 1), v_mean,
                                          statistics.mean(sel), t_dense),
         "clocks": clocks,

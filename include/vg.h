@@ -149,6 +149,46 @@ vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q, const int32_
                               int32_t* error_flag, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Sparse verification, exact merged schedule.
+ * SSV: Sparse Speculative Verification for Efficient LLM Inference, section
+ * 4.2 and Figures 2, 4, 5: each verify row carries its own sparse selection,
+ * and the blocks adjacent rows share are loaded once.
+ *
+ * Row i of sequence b attends the prefix positions of its selected blocks
+ * plus the verify block causally:
+ *   { j < L_b : j / 16 in blocks[b][i][0 .. block_counts[b][i]) }
+ *     u [L_b, L_b + i].
+ * The same selection serves every query head of the sequence.
+ *
+ *   blocks        int32 [batch][n_rows][max_blocks]: 16-position block
+ *                 (logical page) numbers, each < ceil(L_b / 16); order and
+ *                 duplicates do not matter.
+ *   block_counts  int32 [batch][n_rows], 0 <= count <= max_blocks.
+ *   q, prefix_lens, out, num_splits: as vg_verify_attention (no capture).
+ *   workspace     vg_sparse_verify_workspace_bytes(); needs no
+ *                 initialisation.
+ *
+ * Execution: a small kernel forms, per sequence, the ascending union of the
+ * rows' blocks and the verify block's pages, with a row bit per page. The
+ * verify kernel then streams that union once per KV head and masks each row
+ * to its own blocks; a merge kernel follows when there is more than one
+ * split.  Out-of-range blocks (VG_DEVERR_INDEX) and counts (VG_DEVERR_COUNT)
+ * are flagged and skipped.
+ * Supported: as vg_verify_attention, and max_pages_per_seq * 4 <= 200 KB.
+ * ------------------------------------------------------------------------- */
+size_t vg_sparse_verify_workspace_bytes(int batch, int n_rows, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int max_prefix, int max_blocks,
+                                        int num_splits);
+
+vg_status vg_sparse_verify_attention(const vg_paged_kv* kv, const void* q,
+                                     const int32_t* prefix_lens, int batch, int n_rows,
+                                     int num_q_heads, int max_prefix, float softmax_scale,
+                                     const int32_t* blocks, const int32_t* block_counts,
+                                     int max_blocks, void* out, int num_splits, void* workspace,
+                                     size_t workspace_bytes, int32_t* error_flag,
+                                     cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Verification-guided KV selection.
  * Vegas, "Core claim": combine the two captured rows across the query heads
  * and keep the top-k prefix positions.  A Sparse Glimpse of the Whole, "What

@@ -84,6 +84,34 @@ def verify_attention(q, k, v, prefix_lens, scale):
     return out, rows
 
 
+def sparse_verify_attention(q, k, v, prefix_lens, blocks, scale):
+    """Sparse verification: every verify row attends its own selection.
+
+    [SSV] section 4.2 and Figures 2/4/5: each verifier query carries its own
+    sparse layout; the exact merged schedule changes only how shared blocks
+    are loaded, not what each query attends.  Row i of sequence b attends
+    the prefix positions of its 16-position blocks and the verify block
+    causally: {j < L_b : j // 16 in blocks[b][i]} u [L_b, L_b + i] (R25).
+
+    blocks: list over b of lists over rows of block numbers (any order).
+    Returns out [B][R][Hq][d]."""
+    B, R, Hq, d = q.shape
+    Hkv = k[0].shape[0]
+    g = Hq // Hkv
+    out = np.zeros((B, R, Hq, d))
+    for b in range(B):
+        L = int(prefix_lens[b])
+        for i in range(R):
+            sel = sorted(set(int(x) for x in blocks[b][i]))
+            pos = [j for blk in sel for j in range(16 * blk, min(16 * blk + 16, L))]
+            att = np.array(pos + list(range(L, L + i + 1)), dtype=np.int64)
+            for h in range(Hq):
+                kvh = h // g
+                s = scale * (k[b][kvh, att] @ q[b, i, h])
+                out[b, i, h] = _softmax_weights(s) @ v[b][kvh, att]
+    return out
+
+
 def capture_rows(q, k, prefix_lens, scale):
     """Only the Collect-2-Query rows of verify_attention, for large inputs:
     rows[b,h,0,j] = scale*q_{b,0,h}.k_j and rows[b,h,1,j] = scale*q_{b,k,h}.k_j

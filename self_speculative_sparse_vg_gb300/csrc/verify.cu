@@ -56,6 +56,11 @@ struct VerifyParams {
   int max_prefix, max_pages_per_seq, num_pages;
   int capture_mode, splits, tiles_per_split, stages, groups;
   size_t lse_offset;  // VG_CAPTURE_ALL_ROWS: floats before the per-row normalisers
+  // sparse verification: per sequence, the union of the rows' blocks
+  int32_t* u_pages;    // [B][u_max] logical pages, ascending
+  uint32_t* u_masks;   // [B][u_max] bit i: verify row i selected the page
+  int32_t* u_count;    // [B]
+  int u_max;
   float scale, scale_log2;
 };
 
@@ -111,9 +116,10 @@ struct VerifyLayout {
   static constexpr int kCapFloats = 4 * 16 * kCapStride;  // per-warp Collect-2 staging
   static constexpr int kAllFloats = 2 * 4 * kVTile;       // Collect-All partials [slot][warp]
   static constexpr int kBars = 12;                        // besides the ring's 2 per stage
+  static constexpr int kSliceMax = 1024;                  // sparse: union pages of one split
   static size_t bytes(int stages) {
     return 1024 + (size_t)stages * kStageBytes + (size_t)(kCapFloats + kAllFloats) * 4 +
-           (2 * (size_t)stages + kBars) * 8 + 16;
+           (size_t)kSliceMax * 8 + (2 * (size_t)stages + kBars) * 8 + 16;
   }
 };
 
@@ -124,11 +130,12 @@ struct VerifyBars {
 
 // Softmax warp of a copy; COLS = 128 / CS columns of each tile, handled in
 // chunks of 32 (two passes over TMEM when COLS > 32: maximum, then P).
-template <int HD, int COLS, int CM>
+template <int HD, int COLS, int CM, bool SP>
 __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const VerifyBars& bars,
                                                uint8_t* ring, float* cap_s, float* all_s,
-                                               uint32_t tmem, int b, int h, int split, int t0,
-                                               int ntiles, int L, int warp, int lane) {
+                                               const int32_t* sl_page, const uint32_t* sl_mask,
+                                               int sl_n, uint32_t tmem, int b, int h, int split,
+                                               int t0, int ntiles, int L, int warp, int lane) {
   constexpr int CS = kVTile / COLS;       // copies
   constexpr int QC = 4 / CS;              // warps (TMEM quadrants) per copy
   constexpr int RPC = 32 * QC;            // rows per copy
@@ -164,6 +171,29 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
     tc_fence_after();
     const int cpos = tile_pos + col0;  // position of this warp's first column
     const int rem = lim - cpos;        // last attended column of this row among the warp's
+    // sparse: which of this warp's columns the row attends (one bit per column
+    // of each 32-column chunk); the tile's 8 slots hold union pages
+    uint32_t vbits[NCH];
+    if constexpr (SP) {
+#pragma unroll
+      for (int k = 0; k < NCH; ++k) {
+        uint32_t bits = 0;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int slot = lt * (kVTile / kPageSize) + (col0 + k * kChunk) / kPageSize + half;
+          if (m < M && slot < sl_n && sl_page[slot] >= 0) {
+            const int pos0 = sl_page[slot] * kPageSize;
+            const bool sel = (sl_mask[slot] >> ri) & 1u;
+#pragma unroll
+            for (int c = 0; c < kPageSize; ++c) {
+              const int pos = pos0 + c;
+              if (pos < L ? sel : pos <= lim) bits |= 1u << (half * kPageSize + c);
+            }
+          }
+        }
+        vbits[k] = bits;
+      }
+    }
 
     // -------- pass 1: capture (prefix positions) and the row maximum
     float s[kChunk];
@@ -234,7 +264,7 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
       }
 #pragma unroll
       for (int j = 0; j < kChunk; ++j)
-        if (k * kChunk + j <= rem) mx = fmaxf(mx, s[j]);
+        if (SP ? ((vbits[k] >> j) & 1u) != 0 : k * kChunk + j <= rem) mx = fmaxf(mx, s[j]);
     }
     if (cap_all && cpos < L) {
       // across the copy's warps, in order, through shared memory
@@ -299,8 +329,10 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
 #pragma unroll
       for (int j = 0; j < kChunk / 2; ++j) {
         const int jj = k * kChunk + 2 * j;
-        const float p0 = jj <= rem ? ex2(fmaf(s[2 * j], p.scale_log2, nref)) : 0.f;
-        const float p1 = jj + 1 <= rem ? ex2(fmaf(s[2 * j + 1], p.scale_log2, nref)) : 0.f;
+        const bool v0 = SP ? ((vbits[k] >> (2 * j)) & 1u) != 0 : jj <= rem;
+        const bool v1 = SP ? ((vbits[k] >> (2 * j + 1)) & 1u) != 0 : jj + 1 <= rem;
+        const float p0 = v0 ? ex2(fmaf(s[2 * j], p.scale_log2, nref)) : 0.f;
+        const float p1 = v1 ? ex2(fmaf(s[2 * j + 1], p.scale_log2, nref)) : 0.f;
         lsum += p0 + p1;
         pk[k][j] = pack_bf16(p0, p1);
       }
@@ -412,7 +444,7 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
         (mxr + __log2f(lt_all)) * 0.6931471805599453f;
 }
 
-template <int HD, int CM>
+template <int HD, int CM, bool SP>
 __global__ void __launch_bounds__(kVerifyThreads, 1)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const VerifyParams p) {
@@ -436,9 +468,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   uint8_t* ring = smem;
   float* cap_s = reinterpret_cast<float*>(ring + (size_t)stages * kStageBytes);
   float* all_s = cap_s + Lay::kCapFloats;
+  int32_t* sl_page = reinterpret_cast<int32_t*>(all_s + Lay::kAllFloats);  // sparse: split's
+  uint32_t* sl_mask = reinterpret_cast<uint32_t*>(sl_page + Lay::kSliceMax);  // union slice
   VerifyBars bars;
   bars.stages = stages;
-  bars.full = reinterpret_cast<uint64_t*>(all_s + Lay::kAllFloats);
+  bars.full = reinterpret_cast<uint64_t*>(sl_mask + Lay::kSliceMax);
   bars.empty = bars.full + stages;    // P(t) V(t) done: ring stage, S and P buffer free
   bars.s_full = bars.empty + stages;  // S of a buffer computed (tensor-core commit)
   bars.p_full = bars.s_full + 2;      // P of a buffer written by every softmax warp
@@ -454,7 +488,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   // dropped once the length is known).
   constexpr int kPagesPerTile = kVTile / kPageSize;  // 8
   int pre_id = -1;
-  if (warp == kProducerWarp) {
+  if (!SP && warp == kProducerWarp) {
     const int lp = split * p.tiles_per_split * kPagesPerTile + lane;
     if (lp < p.max_pages_per_seq) pre_id = p.page_table[(size_t)b * p.max_pages_per_seq + lp];
   }
@@ -464,10 +498,27 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
     if (threadIdx.x == 0 && split == 0 && h == 0) flag_error(p.error_flag, VG_DEVERR_LENGTH);
     return;  // uniform for every CTA of this sequence
   }
-  const int tiles_b = (n_b + kVTile - 1) / kVTile;
-  const int t0 = split * p.tiles_per_split;
-  const int ntiles = max(0, min(t0 + p.tiles_per_split, tiles_b) - t0);
   const int npages_b = (n_b + kPageSize - 1) / kPageSize;
+  constexpr int kPagesPerTileC = kVTile / kPageSize;
+  const int u_n = SP ? min(p.u_count[b], p.u_max) : 0;  // union pages of this sequence
+  const int tiles_b = SP ? (u_n + kPagesPerTileC - 1) / kPagesPerTileC : (n_b + kVTile - 1) / kVTile;
+  // Dense: split s streams tiles [s tps, (s + 1) tps).  Sparse: the union's
+  // size is known only on the device, so split s takes tiles s, s + S, ...
+  // and every split has work whatever the union's size.
+  const int t0 = SP ? 0 : split * p.tiles_per_split;
+  const int ntiles =
+      SP ? (split < tiles_b ? min((tiles_b - split + p.splits - 1) / p.splits, p.tiles_per_split) : 0)
+         : max(0, min(t0 + p.tiles_per_split, tiles_b) - t0);
+  int sl_n = 0;  // slots of this split's union slice (sparse; -1 past the union)
+  if constexpr (SP) {
+    sl_n = min(ntiles * kPagesPerTileC, Lay::kSliceMax);
+    for (int i = threadIdx.x; i < sl_n; i += kVerifyThreads) {
+      const int lt = i / kPagesPerTileC;
+      const int e = (split + lt * p.splits) * kPagesPerTileC + (i - lt * kPagesPerTileC);
+      sl_page[i] = e < u_n ? p.u_pages[(size_t)b * p.u_max + e] : -1;
+      sl_mask[i] = e < u_n ? p.u_masks[(size_t)b * p.u_max + e] : 0u;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -541,10 +592,13 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
       for (int lt = 0; lt < ntiles; ++lt) {
         if ((lt & 3) == 0) {
           const int lt_l = lt + (lane >> 3);
-          const int lp = (t0 + lt_l) * kPagesPerTile + (lane & 7);
+          const int slot = lt_l * kPagesPerTile + (lane & 7);
+          const int lp = SP ? (slot < sl_n ? sl_page[slot] : -1)
+                            : (t0 + lt_l) * kPagesPerTile + (lane & 7);
           my_id = p.num_pages;  // out of range: TMA fills zeros
-          if (lt_l < ntiles && lp < npages_b) {
-            const int e = lt == 0 ? pre_id : p.page_table[(size_t)b * p.max_pages_per_seq + lp];
+          if (lt_l < ntiles && lp >= 0 && lp < npages_b) {
+            const int e = (lt == 0 && !SP) ? pre_id
+                                           : p.page_table[(size_t)b * p.max_pages_per_seq + lp];
             if (e >= 0 && e < p.num_pages)
               my_id = e;
             else
@@ -637,11 +691,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   } else if (warp < NAW) {
     // ---------------------------------------------------------- softmax
     if (CS == 4)
-      verify_softmax<HD, 32, CM>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
+      verify_softmax<HD, 32, CM, SP>(p, bars, ring, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, warp, lane);
     else if (CS == 2)
-      verify_softmax<HD, 64, CM>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
+      verify_softmax<HD, 64, CM, SP>(p, bars, ring, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, warp, lane);
     else
-      verify_softmax<HD, 128, CM>(p, bars, ring, cap_s, all_s, tmem, b, h, split, t0, ntiles, L, warp, lane);
+      verify_softmax<HD, 128, CM, SP>(p, bars, ring, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, warp, lane);
   }
   tc_fence_before();
   __syncthreads();  // every TMEM access and every MMA of this CTA is done
@@ -677,6 +731,82 @@ __global__ void __launch_bounds__(kMergeThreads) verify_merge_kernel(const Verif
                        ? p.capture + p.lse_offset +
                              ((size_t)b * p.num_q_heads + h * p.group + qi) * p.n_rows + i
                        : nullptr);
+}
+
+// Sparse verification, exact merged schedule (SSV: Sparse Speculative
+// Verification, section 4.2 and Figures 2/4/5): the union of the verify rows'
+// selected blocks (16-position pages) plus the pages of the verify block
+// itself, ascending, with one bit per row that selected each page.  One CTA
+// per sequence: page bits in shared memory, then an ordered compaction.
+constexpr int kUnionThreads = 1024;
+
+__global__ void __launch_bounds__(kUnionThreads)
+    sparse_union_kernel(const VerifyParams p, const int32_t* blocks, const int32_t* block_counts,
+                        int max_blocks) {
+  extern __shared__ uint32_t pm[];  // [pages of the sequence] row bits
+  __shared__ int wsum[32], woff[32], tot_s, base_s;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int R = p.n_rows;
+  const int L = p.prefix_lens[b];
+  if (L < 1 || L > p.max_prefix || (L + R + kPageSize - 1) / kPageSize > p.max_pages_per_seq) {
+    if (tid == 0) p.u_count[b] = 0;  // the verify kernel skips and flags the sequence
+    return;
+  }
+  const int npb = (L + R + kPageSize - 1) / kPageSize;  // pages up to the end of the block
+  const int npl = (L + kPageSize - 1) / kPageSize;      // pages holding prefix positions
+  for (int i = tid; i < npb; i += kUnionThreads) pm[i] = 0;
+  __syncthreads();
+  for (int e = tid; e < R * max_blocks; e += kUnionThreads) {
+    const int i = e / max_blocks, k = e - i * max_blocks;
+    const int cnt = block_counts[(size_t)b * R + i];
+    if (cnt < 0 || cnt > max_blocks) {
+      if (k == 0) flag_error(p.error_flag, VG_DEVERR_COUNT);
+      continue;
+    }
+    if (k >= cnt) continue;
+    const int blk = blocks[((size_t)b * R + i) * max_blocks + k];
+    if (blk < 0 || blk >= npl) {
+      flag_error(p.error_flag, VG_DEVERR_INDEX);
+      continue;
+    }
+    atomicOr(&pm[blk], 1u << i);
+  }
+  for (int pg = L / kPageSize + tid; pg < npb; pg += kUnionThreads)
+    atomicOr(&pm[pg], 1u << 31);  // the verify block's own pages are always streamed
+  if (tid == 0) base_s = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < npb; c0 += kUnionThreads) {
+    const int pg = c0 + tid;
+    const bool f = pg < npb && pm[pg] != 0u;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) wsum[wid] = __popc(bal);
+    __syncthreads();
+    if (wid == 0) {
+      const int v = wsum[lane];
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      woff[lane] = incl - v;
+      if (lane == 31) tot_s = incl;
+    }
+    __syncthreads();
+    if (f) {
+      const int slot = base_s + woff[wid] + __popc(bal & ((1u << lane) - 1u));
+      if (slot < p.u_max) {
+        p.u_pages[(size_t)b * p.u_max + slot] = pg;
+        p.u_masks[(size_t)b * p.u_max + slot] = pm[pg] & 0xffffu;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) base_s += tot_s;
+    __syncthreads();
+  }
+  if (tid == 0) p.u_count[b] = min(base_s, p.u_max);
 }
 
 struct VerifyPlan {
@@ -723,14 +853,14 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   return true;
 }
 
-template <int HD, int CM>
+template <int HD, int CM, bool SP = false>
 cudaError_t launch_verify_main(const VerifyPlan& pl, const CUtensorMap& tk, const CUtensorMap& tv,
                                const VerifyParams& p, dim3 grid, cudaStream_t stream) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel<HD, CM>,
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<HD, CM, SP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -745,14 +875,17 @@ cudaError_t launch_verify_main(const VerifyPlan& pl, const CUtensorMap& tk, cons
   vcfg.stream = stream;
   vcfg.attrs = pdl;
   vcfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&vcfg, verify_kernel<HD, CM>, tk, tv, p);
+  return cudaLaunchKernelEx(&vcfg, verify_kernel<HD, CM, SP>, tk, tv, p);
 }
 
 template <int HD>
 cudaError_t launch_verify(const VerifyPlan& pl, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const VerifyParams& p, dim3 grid, cudaStream_t stream) {
+                          const VerifyParams& p, dim3 grid, cudaStream_t stream,
+                          bool sparse = false) {
   cudaError_t e;
-  switch (p.capture_mode) {
+  if (sparse) {
+    e = launch_verify_main<HD, VG_CAPTURE_NONE, true>(pl, tk, tv, p, grid, stream);
+  } else switch (p.capture_mode) {
     case VG_CAPTURE_GROUP_SUM: e = launch_verify_main<HD, VG_CAPTURE_GROUP_SUM>(pl, tk, tv, p, grid, stream); break;
     case VG_CAPTURE_ROWS: e = launch_verify_main<HD, VG_CAPTURE_ROWS>(pl, tk, tv, p, grid, stream); break;
     case VG_CAPTURE_ALL_SUM: e = launch_verify_main<HD, VG_CAPTURE_ALL_SUM>(pl, tk, tv, p, grid, stream); break;
@@ -822,7 +955,7 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
       !page_pool_tensor_map(kv->v_pages, kv->num_pages, kv->num_kv_heads, kv->head_dim, &tv))
     return VG_ERR_LAUNCH;
 
-  VerifyParams p;
+  VerifyParams p = {};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.prefix_lens = prefix_lens;
   p.page_table = kv->page_table;
@@ -853,6 +986,152 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
   dim3 grid(pl.splits, kv->num_kv_heads, batch);
   const cudaError_t e = kv->head_dim == 128 ? launch_verify<128>(pl, tk, tv, p, grid, stream)
                                              : launch_verify<64>(pl, tk, tv, p, grid, stream);
+  return e == cudaSuccess ? VG_OK : VG_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Sparse verification (declared in vg.h).
+namespace {
+
+// Most union pages a sequence can have: every row's blocks distinct, plus the
+// pages of the verify block, never more than the pages of the whole range.
+int sparse_union_max(int max_prefix, int n_rows, int max_blocks) {
+  const long long all = ceil_div(max_prefix + n_rows, kPageSize);
+  const long long sel = (long long)n_rows * max_blocks + ceil_div(n_rows, kPageSize) + 1;
+  return (int)std::min(all, sel);
+}
+
+struct SparseLayout {
+  VerifyPlan pl;
+  int u_max;
+  size_t off_pages, off_masks, off_count, bytes;
+};
+
+bool make_sparse_layout(int batch, int n_rows, int num_q_heads, int num_kv_heads, int head_dim,
+                        int max_prefix, int max_blocks, int num_splits, SparseLayout* sl) {
+  if (max_blocks < 0 || max_prefix <= 0 || n_rows <= 0) return false;
+  sl->u_max = std::max(1, sparse_union_max(max_prefix, n_rows, max_blocks));
+  // plan the splits over the largest union, as if it were a dense range
+  const int eff = std::max(1, sl->u_max * kPageSize - n_rows);
+  if (!make_verify_plan(batch, n_rows, num_q_heads, num_kv_heads, head_dim, eff, num_splits,
+                        &sl->pl))
+    return false;
+  // a split's union pages must fit its shared-memory slice
+  constexpr int kMaxTps = VerifyLayout<128>::kSliceMax / (kVTile / kPageSize);
+  if (sl->pl.tiles_per_split > kMaxTps) {
+    const int tiles = ceil_div(eff + n_rows, kVTile);
+    if (!make_verify_plan(batch, n_rows, num_q_heads, num_kv_heads, head_dim, eff,
+                          std::max(num_splits, ceil_div(tiles, kMaxTps)), &sl->pl))
+      return false;
+    if (sl->pl.tiles_per_split > kMaxTps) return false;
+  }
+  sl->off_pages = align_up(sl->pl.ws_bytes, 256);
+  sl->off_masks = sl->off_pages + align_up((size_t)batch * sl->u_max * 4, 256);
+  sl->off_count = sl->off_masks + align_up((size_t)batch * sl->u_max * 4, 256);
+  sl->bytes = sl->off_count + align_up((size_t)batch * 4, 256);
+  return true;
+}
+
+}  // namespace
+
+extern "C" size_t vg_sparse_verify_workspace_bytes(int batch, int n_rows, int num_q_heads,
+                                                   int num_kv_heads, int head_dim, int max_prefix,
+                                                   int max_blocks, int num_splits) {
+  SparseLayout sl;
+  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      !make_sparse_layout(batch, n_rows, num_q_heads, num_kv_heads, head_dim, max_prefix,
+                          max_blocks, num_splits, &sl))
+    return 0;
+  return sl.bytes;
+}
+
+extern "C" vg_status vg_sparse_verify_attention(
+    const vg_paged_kv* kv, const void* q, const int32_t* prefix_lens, int batch, int n_rows,
+    int num_q_heads, int max_prefix, float softmax_scale, const int32_t* blocks,
+    const int32_t* block_counts, int max_blocks, void* out, int num_splits, void* workspace,
+    size_t workspace_bytes, int32_t* error_flag, cudaStream_t stream) {
+  vg_status st = check_paged_kv(kv);
+  if (st != VG_OK) return st;
+  if (!q || !prefix_lens || !out || !block_counts || batch <= 0 || n_rows <= 0 ||
+      num_q_heads <= 0 || max_prefix <= 0 || num_splits < 0 || max_blocks < 0 ||
+      !(softmax_scale == softmax_scale) || (max_blocks > 0 && !blocks))
+    return VG_ERR_INVALID_ARGUMENT;
+  if (num_q_heads % kv->num_kv_heads) return VG_ERR_INVALID_ARGUMENT;
+  const int g = num_q_heads / kv->num_kv_heads;
+  if (g > 8 || n_rows > 16 || g * n_rows > 96) return VG_ERR_UNSUPPORTED;
+  if (ceil_div(max_prefix + n_rows, kPageSize) > kv->max_pages_per_seq)
+    return VG_ERR_INVALID_ARGUMENT;
+  if ((size_t)kv->max_pages_per_seq * 4 > 200 * 1024) return VG_ERR_UNSUPPORTED;
+  SparseLayout sl;
+  if (!make_sparse_layout(batch, n_rows, num_q_heads, kv->num_kv_heads, kv->head_dim, max_prefix,
+                          max_blocks, num_splits, &sl))
+    return VG_ERR_INVALID_ARGUMENT;
+  if (!workspace || workspace_bytes < sl.bytes) return VG_ERR_WORKSPACE_TOO_SMALL;
+  if (sl.pl.smem_bytes > 227 * 1024) return VG_ERR_UNSUPPORTED;
+  CUtensorMap tk, tv;
+  if (!page_pool_tensor_map(kv->k_pages, kv->num_pages, kv->num_kv_heads, kv->head_dim, &tk) ||
+      !page_pool_tensor_map(kv->v_pages, kv->num_pages, kv->num_kv_heads, kv->head_dim, &tv))
+    return VG_ERR_LAUNCH;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  VerifyParams p = {};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.prefix_lens = prefix_lens;
+  p.page_table = kv->page_table;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.capture = nullptr;
+  p.part_o = sl.pl.ws_bytes ? reinterpret_cast<float*>(ws) : nullptr;
+  p.part_ml = sl.pl.ws_bytes ? reinterpret_cast<float*>(ws + sl.pl.off_ml) : nullptr;
+  p.error_flag = error_flag;
+  p.batch = batch;
+  p.n_rows = n_rows;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = kv->num_kv_heads;
+  p.group = g;
+  p.m_rows = sl.pl.m_rows;
+  p.m_tiles = sl.pl.m_tiles;
+  p.max_prefix = max_prefix;
+  p.max_pages_per_seq = kv->max_pages_per_seq;
+  p.num_pages = kv->num_pages;
+  p.capture_mode = VG_CAPTURE_NONE;
+  p.lse_offset = 0;
+  p.splits = sl.pl.splits;
+  p.tiles_per_split = sl.pl.tiles_per_split;
+  p.stages = sl.pl.stages;
+  p.groups = sl.pl.groups;
+  p.u_pages = reinterpret_cast<int32_t*>(ws + sl.off_pages);
+  p.u_masks = reinterpret_cast<uint32_t*>(ws + sl.off_masks);
+  p.u_count = reinterpret_cast<int32_t*>(ws + sl.off_count);
+  p.u_max = sl.u_max;
+  p.scale = softmax_scale;
+  p.scale_log2 = softmax_scale * kLog2e;
+  // the union pass, then the verify grid and its split merge (PDL chain)
+  const size_t usmem = (size_t)kv->max_pages_per_seq * 4;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(sparse_union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             200 * 1024) != cudaSuccess)
+      return VG_ERR_LAUNCH;
+    attr_done[dev] = true;
+  }
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t ucfg = {};
+  ucfg.gridDim = dim3(batch, 1, 1);
+  ucfg.blockDim = dim3(kUnionThreads, 1, 1);
+  ucfg.dynamicSmemBytes = usmem;
+  ucfg.stream = stream;
+  ucfg.attrs = pdl;
+  ucfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&ucfg, sparse_union_kernel, p, blocks, block_counts, max_blocks) !=
+      cudaSuccess)
+    return VG_ERR_LAUNCH;
+  dim3 grid(sl.pl.splits, kv->num_kv_heads, batch);
+  const cudaError_t e = kv->head_dim == 128
+                            ? launch_verify<128>(sl.pl, tk, tv, p, grid, stream, true)
+                            : launch_verify<64>(sl.pl, tk, tv, p, grid, stream, true);
   return e == cudaSuccess ? VG_OK : VG_ERR_LAUNCH;
 }
 

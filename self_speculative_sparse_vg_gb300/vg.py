@@ -33,6 +33,7 @@ EXPORTED = (
     "vg_sparse_draft_workspace_bytes", "vg_sparse_draft_attention",
     "vg_status_string", "vg_version",
     "vg_verify_noalloc_scratch_bytes", "vg_verify_attention_noalloc",
+    "vg_sparse_verify_workspace_bytes", "vg_sparse_verify_attention",
 )
 
 
@@ -71,6 +72,9 @@ def _load():
         "vg_verify_noalloc_scratch_bytes": (sz, []),
         "vg_verify_attention_noalloc": (i32, [kvp, vp, vp, i32, i32, i32, i32, f32, vp, i32, vp,
                                               i32, vp, vp]),
+        "vg_sparse_verify_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32, i32]),
+        "vg_sparse_verify_attention": (i32, [kvp, vp, vp, i32, i32, i32, i32, f32, vp, vp, i32, vp,
+                                             i32, vp, sz, vp, vp]),
         "vg_status_string": (ctypes.c_char_p, [i32]),
         "vg_version": (ctypes.c_char_p, []),
     }
@@ -168,6 +172,33 @@ def verify_attention_noalloc(kv: PagedKV, q, prefix_lens, max_prefix, softmax_sc
                                          int(capture_mode), _ptr(capture), int(num_splits),
                                          _ptr(error_flag), _stream(stream))
     _check("vg_verify_attention_noalloc", s)
+    return out
+
+
+def sparse_verify_workspace_bytes(batch, n_rows, num_q_heads, num_kv_heads, head_dim, max_prefix,
+                                  max_blocks, num_splits=0) -> int:
+    return int(_lib.vg_sparse_verify_workspace_bytes(batch, n_rows, num_q_heads, num_kv_heads,
+                                                     head_dim, max_prefix, max_blocks, num_splits))
+
+
+def sparse_verify_attention(kv: PagedKV, q, prefix_lens, max_prefix, softmax_scale, blocks,
+                            block_counts, out, num_splits=0, workspace=None, error_flag=None,
+                            stream=None):
+    """vg_sparse_verify_attention.  blocks int32 [B][R][max_blocks] (16-position
+    prefix blocks per verify row), block_counts int32 [B][R]."""
+    B, R, Hq, d = q.shape
+    max_blocks = blocks.shape[-1]
+    if workspace is None:
+        workspace = zero_workspace(sparse_verify_workspace_bytes(
+            B, R, Hq, kv.num_kv_heads, d, max_prefix, max_blocks, num_splits), q.device)
+    st = kv.struct()
+    s = _lib.vg_sparse_verify_attention(ctypes.byref(st), _ptr(q), _ptr(prefix_lens), B, R, Hq,
+                                        int(max_prefix), float(softmax_scale), _ptr(blocks),
+                                        _ptr(block_counts), int(max_blocks), _ptr(out),
+                                        int(num_splits), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _ptr(error_flag), _stream(stream))
+    _check("vg_sparse_verify_attention", s)
     return out
 
 

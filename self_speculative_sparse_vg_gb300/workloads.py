@@ -350,3 +350,33 @@ def make_acceptance(spec: StackSpec) -> torch.Tensor:
     speculative sampling, which need a trained model."""
     g = torch.Generator().manual_seed(spec.seed * 7919 - 2)
     return torch.rand(spec.iterations, spec.batch, spec.n_drafts, generator=g) < spec.accept_p
+
+
+def make_block_selection(spec: WorkloadSpec, frac: float, seed: int, overlap: float = 0.75):
+    """Per verify row, a seeded set of 16-position prefix blocks for sparse
+    verification: a core shared by all rows of the sequence (a share
+    `overlap` of each row's blocks) plus row-private blocks, so adjacent rows
+    overlap the way speculative rows do.  frac is the fraction of the
+    sequence's prefix blocks a row selects (0 selects none, 1 all).
+    Returns (blocks int32 [B][R][max_blocks] padded with -1, counts int32 [B][R])."""
+    g = torch.Generator().manual_seed(seed)
+    B, R = spec.batch, spec.n_rows
+    nbl = [(L + PAGE_SIZE - 1) // PAGE_SIZE for L in spec.prefix_lens]
+    want = [min(n, int(round(frac * n))) for n in nbl]
+    max_blocks = max(1, max(want))
+    blocks = torch.full((B, R, max_blocks), -1, dtype=torch.int32)
+    counts = torch.zeros(B, R, dtype=torch.int32)
+    for b, n in enumerate(nbl):
+        w = want[b]
+        core = torch.randperm(n, generator=g)[:int(round(w * overlap))].tolist()
+        for i in range(R):
+            sel = list(core)
+            for x in torch.randperm(n, generator=g).tolist():
+                if len(sel) >= w:
+                    break
+                if x not in sel:
+                    sel.append(x)
+            sel = sorted(sel)
+            blocks[b, i, :len(sel)] = torch.tensor(sel, dtype=torch.int32) if sel else blocks[b, i, :0]
+            counts[b, i] = len(sel)
+    return blocks, counts

@@ -408,3 +408,36 @@ def test_weight_selection_ranks_like_logits_for_one_row_and_head():
     b_ = O.select_kv(rows, O.CAPTURE_ROWS, [200, 77], 1, 1, 20, 2, 5, False)
     for x, y in zip(a, b_):
         assert x[0].tolist() == y[0].tolist()
+
+
+def test_sparse_verify_with_every_block_is_dense_verify():
+    """Selecting every prefix block reproduces full verification; selecting
+    none leaves only the causal block."""
+    rng = np.random.default_rng(61)
+    q, k, v = _rand_case(rng, 2, 3, 4, 2, 8, [37, 16])
+    full = [[list(range((L + 15) // 16)) for _ in range(3)] for L in (37, 16)]
+    dense, _ = O.verify_attention(q, k, v, [37, 16], 0.4)
+    np.testing.assert_allclose(O.sparse_verify_attention(q, k, v, [37, 16], full, 0.4), dense,
+                               rtol=0, atol=1e-12)
+    none = [[[] for _ in range(3)] for _ in range(2)]
+    got = O.sparse_verify_attention(q, k, v, [37, 16], none, 0.4)
+    # row 0 with no blocks attends only its own position: its V row
+    for b, L in enumerate((37, 16)):
+        for h in range(4):
+            np.testing.assert_allclose(got[b, 0, h], v[b][h // 2, L], rtol=0, atol=1e-12)
+
+
+def test_sparse_verify_equals_masked_textbook_attention():
+    """A brute-force mask over the full causal score matrix."""
+    rng = np.random.default_rng(62)
+    q, k, v = _rand_case(rng, 1, 4, 2, 1, 8, [70])
+    blocks = [[[0, 3], [1], [4, 0, 2], []]]
+    got = O.sparse_verify_attention(q, k, v, [70], blocks, 0.3)
+    for i in range(4):
+        allowed = [j for j in range(70) if j // 16 in blocks[0][i]] + list(range(70, 70 + i + 1))
+        for h in range(2):
+            S = 0.3 * (k[0][0] @ q[0, i, h])                 # every position of the sequence
+            mask = np.full(S.shape, -np.inf)
+            mask[allowed] = 0.0
+            w = sp_softmax(S + mask)
+            np.testing.assert_allclose(got[0, i, h], w @ v[0][0], rtol=0, atol=1e-12)
