@@ -537,9 +537,9 @@ def main():
         tail = set(range(L // 16, (L + R_ + 15) // 16))
         u = set(tail)
         for i in range(R_):
-            sel = set(blocks[b_i, i, :int(counts[b_i, i])].tolist())
-            u |= sel
-            rows_sum += len(sel | tail)
+            row_blocks = set(blocks[b_i, i, :int(counts[b_i, i])].tolist())
+            u |= row_blocks
+            rows_sum += len(row_blocks | tail)
         union += len(u)
     page_bytes = spec.num_kv_heads * 16 * spec.head_dim * 2 * 2
     sparse_study = {

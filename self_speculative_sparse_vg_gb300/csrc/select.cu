@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kSelThreads = 1024;
 constexpr int kMaxCluster = 16;
-constexpr int kTargetSlice = 4096;
+constexpr int kTargetSlice = 2048;
 constexpr int kMaxSlice = 16384;  // keys per CTA (64 KB of shared memory)
 
 struct SelectParams {
