@@ -13,10 +13,10 @@
 //  * The chunk's selected positions, the sequence's page-table row (one bulk
 //    copy into shared memory when short), the query rows and the lengths are
 //    loaded together, so a row's address costs one round trip.
-//  * Each of the chunk's K and V rows (256 bytes at head_dim 128) is then one
-//    bulk copy (cp.async.bulk, completion counted on an mbarrier with a
-//    bounded wait) into a row-padded tile (row stride head_dim * 2 + 16
-//    bytes, so ldmatrix rows fall in distinct bank groups).
+//  * The chunk's K and V rows (256 bytes each at head_dim 128) are then
+//    gathered with 16-byte cp.async pieces, consecutive threads on
+//    consecutive pieces of a row, into a row-padded tile (row stride
+//    head_dim * 2 + 16 bytes, so ldmatrix rows fall in distinct bank groups).
 //  * The g query heads of the KV head are the rows of a 16-row bf16
 //    mma.sync tile (zero padded); warp w takes positions [16w, 16w + 16),
 //    and P is reused as the A operand of P.V.
@@ -103,13 +103,12 @@ __global__ void __launch_bounds__(kDraftThreads)
   uint8_t* vt = kt + Lay::kTileBytes;
   uint8_t* qs = vt + Lay::kTileBytes;  // [16][RB]
   int32_t* pt_s = reinterpret_cast<int32_t*>(qs + Lay::kQBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(pt_s + kPtMax);  // [0] page table, [1] K/V rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pt_s + kPtMax);  // [0] page table
   __shared__ long long off_s[kChunk];
   __shared__ float wm_s[kDraftWarps][16], wl_s[kDraftWarps][16];
 
   if (tid == 0) {
     mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], kChunk);  // one arrival per row thread
     fence_barrier_init();
   }
   __syncthreads();
@@ -186,21 +185,29 @@ __global__ void __launch_bounds__(kDraftThreads)
       }
     }
     off_s[tid] = off;
-    uint8_t* kd = kt + tid * RB;
-    uint8_t* vd = vt + tid * RB;
-    if (off >= 0) {
-      mbar_arrive_expect_tx(&bars[1], 2 * HD * 2);
-      bulk_load(kd, p.k_pages + off, HD * 2, &bars[1]);
-      bulk_load(vd, p.v_pages + off, HD * 2, &bars[1]);
-    } else {
+    if (off < 0) {
+      uint8_t* kd = kt + tid * RB;
+      uint8_t* vd = vt + tid * RB;
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
         *reinterpret_cast<uint4*>(kd + c * 16) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(vd + c * 16) = make_uint4(0, 0, 0, 0);
       }
-      mbar_arrive(&bars[1]);
     }
   }
+  __syncthreads();  // every row's offset is known
+  // gather: 16-byte cp.async pieces, consecutive threads on consecutive
+  // pieces of a row (K rows, then V rows), all in flight at once
+#pragma unroll 4
+  for (int idx = tid; idx < 2 * kChunk * CH; idx += kDraftThreads) {
+    const int t = idx / (kChunk * CH);
+    const int rem = idx - t * (kChunk * CH);
+    const int rr = rem / CH, ch = rem - rr * CH;
+    const long long off = off_s[rr];
+    if (off >= 0)
+      cp_async_16((t ? vt : kt) + rr * RB + ch * 16, (t ? p.v_pages : p.k_pages) + off + ch * 8);
+  }
+  cp_async_commit();
   // Q fragments while the rows are in flight
   const uint32_t qs_u = smem_u32(qs);
   uint32_t qa[KS][4];
@@ -211,8 +218,8 @@ __global__ void __launch_bounds__(kDraftThreads)
       ldsm_x4(qs_u + qrow * RB + (2 * ks + (lane >> 4)) * 16, qa[ks][0], qa[ks][1], qa[ks][2],
               qa[ks][3]);
   }
-  if (!mbar_wait(&bars[1], 0)) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-  __syncthreads();  // zero rows and off_s written by other threads
+  cp_async_wait<0>();
+  __syncthreads();  // every thread's pieces have landed
 
   // warp w: positions [16w, 16w + 16) of the chunk
   const int r = lane >> 2, c = lane & 3;

@@ -40,6 +40,10 @@ SMALL = dict(
     short=dict(prefix_lens=(1, 15, 16, 63, 64, 65, 130), batch=7, top_k=8, n_sink=2, n_recent=4),
     budget_all=dict(prefix_lens=(40, 83), top_k=64, n_sink=4, n_recent=16),
     ties=dict(prefix_lens=(700,), batch=1, top_k=33),
+    # batch * KV heads > 16: 64-entry chunks, one CTA each, and the merge kernel
+    many_pairs=dict(batch=3, prefix_lens=(1000, 517, 333), num_q_heads=32, num_kv_heads=8),
+    # a list longer than one 16-CTA cluster covers: cluster partials + merge kernel
+    long_list=dict(batch=1, prefix_lens=(6000,), num_q_heads=4, num_kv_heads=1, top_k=5500),
 )
 
 
@@ -180,17 +184,21 @@ def test_poisoned_workspace_and_repeat():
     assert torch.equal(st.out_draft, ref_d)
 
 
-def test_draft_graph_replay_eager_and_empty_list():
+@pytest.mark.parametrize("kw", [dict(prefix_lens=(3000, 900)),
+                                dict(batch=1, prefix_lens=(6000,), num_q_heads=4, num_kv_heads=1,
+                                     top_k=5500)], ids=["cluster", "multi_cluster"])
+def test_draft_graph_replay_eager_and_empty_list(kw):
     """A captured graph of the draft steps replayed several times and eager
-    calls after it are bit-identical to the first eager run; an empty
-    attended list gives zeros."""
+    calls after it are bit-identical to the first eager run, also on a
+    NaN-poisoned workspace; an empty attended list gives zeros."""
     _require_gpu()
     from self_speculative_sparse_vg_gb300.step import DecodeStep
     from self_speculative_sparse_vg_gb300.workloads import make_inputs, small_spec
-    inp = make_inputs(small_spec(prefix_lens=(3000, 900)))
+    inp = make_inputs(small_spec(**kw))
     st = DecodeStep.create(inp, "cuda")
     st.run()
     ref = st.out_draft.clone()
+    st.ws_draft.fill_(0xFF)   # NaN bit patterns in every partial
     k = st.spec.n_drafts
     graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
