@@ -6,19 +6,22 @@
 // the Whole, "What carries the argument": sink and recent tokens are always
 // kept; per-head index variant.
 //
-// Design: a score kernel, spread over many CTAs, forms every position's fp32
-// score in the documented order and stores its order-preserving 32-bit key in
-// the workspace.  Then one thread-block cluster of C (<= 16) CTAs per
-// selection row: CTA c loads the keys of a contiguous slice of positions into
-// shared memory and takes part in an MSB-first 8-bit radix select (at most 4
-// passes, fewer once the whole boundary bin is kept) whose 256-bin
-// histograms are summed across the cluster through distributed shared memory
-// (double-buffered, one cluster barrier per pass).  That yields the exact
-// top_k-th key T.  Keys > T are all kept; keys == T are kept by ascending
-// position, using exclusive per-CTA counts exchanged across the cluster; each
-// CTA then writes its kept positions in order straight into their final
-// slots.  The result is deterministic and equals a stable sort by
-// (score desc, position asc).
+// Design: one thread-block cluster of C (<= 16) CTAs per selection row; CTA c
+// owns a contiguous slice of positions.  Each position's fp32 score is formed
+// in the documented order and turned into an order-preserving 32-bit key:
+// for the per-KV-head sum captures, when a CTA's share is at most 16K loads,
+// by the cluster's CTAs themselves, straight into shared memory; otherwise
+// (longer prefixes, raw-row and attention-weight captures) by a score kernel
+// spread over many CTAs, through the workspace.  The cluster then runs an
+// MSB-first 8-bit radix select (at most 4 passes, fewer once the whole
+// boundary bin is kept): every CTA pushes its 256-bin histogram into every
+// CTA's shared memory with st.async, each CTA waits on a local mbarrier for
+// the C histograms and sums them itself (no cluster barrier per pass).  That
+// yields the exact top_k-th key T.  Keys > T are all kept; keys == T are kept
+// by ascending position, using per-CTA counts pushed the same way; each CTA
+// then writes its kept positions in order straight into their final slots.
+// The result is deterministic and equals a stable sort by (score desc,
+// position asc).
 #include <cooperative_groups.h>
 
 #include "vg_device.cuh"
@@ -33,9 +36,11 @@ constexpr int kSelThreads = 1024;
 constexpr int kMaxCluster = 16;
 constexpr int kTargetSlice = 2048;
 constexpr int kMaxSlice = 16384;  // keys per CTA (64 KB of shared memory)
+constexpr int kFusedLoads = 16384;  // capture loads per CTA up to which the cluster scores
 
 struct SelectParams {
   const float* capture;
+  int fused;          // keys formed in the select kernel (per-KV-head sum captures)
   uint32_t* keys_ws;  // [B][rows][max_prefix] order-preserving score keys
   const int32_t* prefix_lens;
   int32_t* indices;
@@ -59,6 +64,24 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 // of one position are all issued before the first add (batches of 16), so a
 // score costs one memory round trip per batch rather than one per term.
 constexpr int kLoadBatch = 16;
+
+// Per-KV-head sum capture: the row's own KV head, or the sum over KV heads.
+__device__ __forceinline__ float group_sum_score(const SelectParams& p, int b, int row, int j) {
+  const size_t L = p.max_prefix;
+  const float* G = p.capture + (size_t)b * p.num_kv_heads * L + j;
+  if (p.per_head) return __ldg(G + (size_t)row * L);
+  float acc = 0.f;
+  for (int h0 = 0; h0 < p.num_kv_heads; h0 += kLoadBatch) {
+    float v[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      v[u] = (h0 + u < p.num_kv_heads) ? __ldg(G + (size_t)(h0 + u) * L) : 0.f;
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u)
+      if (h0 + u < p.num_kv_heads) acc = (h0 + u == 0) ? v[u] : acc + v[u];
+  }
+  return acc;
+}
 
 __device__ __forceinline__ float row_score(const SelectParams& p, int b, int row, int j) {
   const size_t L = p.max_prefix;
@@ -91,21 +114,7 @@ __device__ __forceinline__ float row_score(const SelectParams& p, int b, int row
     }
     return acc;
   }
-  if (p.capture_mode == VG_CAPTURE_GROUP_SUM) {
-    const float* G = p.capture + (size_t)b * p.num_kv_heads * L + j;
-    if (p.per_head) return __ldg(G + (size_t)row * L);
-    float acc = 0.f;
-    for (int h0 = 0; h0 < p.num_kv_heads; h0 += kLoadBatch) {
-      float v[kLoadBatch];
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u)
-        v[u] = (h0 + u < p.num_kv_heads) ? __ldg(G + (size_t)(h0 + u) * L) : 0.f;
-#pragma unroll
-      for (int u = 0; u < kLoadBatch; ++u)
-        if (h0 + u < p.num_kv_heads) acc = (h0 + u == 0) ? v[u] : acc + v[u];
-    }
-    return acc;
-  }
+  if (p.capture_mode == VG_CAPTURE_GROUP_SUM) return group_sum_score(p, b, row, j);
   const float* Rw = p.capture + (size_t)b * p.num_q_heads * 2 * L + j;  // [q][2][L]
   const int g = p.group;  // <= 8, so one KV head's 2g terms fit one batch
   const int h0 = p.per_head ? row : 0, h1 = p.per_head ? row + 1 : p.num_kv_heads;
@@ -145,12 +154,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   const int row = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31;
 
-  __shared__ uint32_t hist[2][256];
+  __shared__ __align__(16) uint32_t hist[2][256];
   __shared__ uint32_t tot_s[256];
   __shared__ int cnt[2];    // this CTA's candidate keys > T and == T
   __shared__ int ctl[5];    // digit, remaining k, gt_before, eq_before, boundary-bin count
   __shared__ int wb[160];
-  extern __shared__ __align__(16) uint32_t keys[];  // [slice]
+  // dynamic: keys [slice], then the histograms pushed by the cluster's CTAs
+  // [pass][CTA][256], the counts they push [CTA] (uint4), and 5 mbarriers
+  // counting the pushed bytes (one per pass, one for the counts)
+  extern __shared__ __align__(16) uint8_t sel_smem[];
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sel_smem);
+  uint32_t* recv = reinterpret_cast<uint32_t*>(sel_smem + ((p.slice * 4 + 15) & ~15));
+  uint4* crecv = reinterpret_cast<uint4*>(recv + 4 * kMaxCluster * 256);
+  uint64_t* mb = reinterpret_cast<uint64_t*>(crecv + kMaxCluster);
 
   // programmatic dependent launch: the capture comes from the previous kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -175,9 +191,28 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   }
   const int c_lo = p.n_sink, c_hi = L - p.n_recent;  // candidates [c_lo, c_hi)
 
-  const uint32_t* kw = p.keys_ws + ((size_t)b * p.rows + row) * p.max_prefix + lo;
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(&mb[i], 1);
+    fence_barrier_init();
+    for (int i = 0; i < 4; ++i) mbar_arrive_expect_tx(&mb[i], (uint32_t)C * 1024u);
+    mbar_arrive_expect_tx(&mb[4], (uint32_t)C * 16u);
+  }
+  __syncthreads();
+  // once this barrier completes, every CTA's mbarriers are initialised and
+  // may receive pushes; its wait comes just before the first push
+  cluster_arrive_relaxed();
+  bool peers_ready = false;
+
+  if (tid < 256) hist[0][tid] = 0;  // the first pass's histogram
+  if (p.fused) {
+#pragma unroll 2
+    for (int j = tid; j < n_loc; j += blockDim.x)
+      keys[j] = score_key(group_sum_score(p, b, row, lo + j));
+  } else {
+    const uint32_t* kw = p.keys_ws + ((size_t)b * p.rows + row) * p.max_prefix + lo;
 #pragma unroll 4
-  for (int j = tid; j < n_loc; j += blockDim.x) keys[j] = __ldcg(kw + j);
+    for (int j = tid; j < n_loc; j += blockDim.x) keys[j] = __ldcg(kw + j);
+  }
   __syncthreads();
 
   // ---- exact top_k-th largest candidate key: 4 passes of 8 bits, MSB first
@@ -187,9 +222,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   if (p.top_k > 0) {
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      uint32_t* hb = hist[pass & 1];
-      if (tid < 256) hb[tid] = 0;
-      __syncthreads();
+      uint32_t* hb = hist[pass & 1];  // zeroed, with a barrier since
       for (int it = 0; it < iters; ++it) {
         const int j = it * blockDim.x + tid;
         const int pos = lo + j;
@@ -200,15 +233,30 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
         const unsigned grp = __match_any_sync(0xffffffffu, dig);
         if (v && lane == __ffs(grp) - 1) atomicAdd(&hb[dig], (uint32_t)__popc(grp));
       }
-      cluster.sync();
-      if (tid < 256) {  // all C remote loads issued before any is used
+      __syncthreads();
+      if (!peers_ready) {
+        cluster_wait_acquire();
+        peers_ready = true;
+      }
+      // push this CTA's histogram (64 pieces of 16 bytes) into slot `rank` of
+      // every CTA's region for this pass
+      uint32_t* rp = recv + pass * kMaxCluster * 256;
+      if (tid < 64 * C) {
+        const int dst = tid >> 6, piece = tid & 63;
+        const uint4 hv = reinterpret_cast<const uint4*>(hb)[piece];
+        st_async_v4(mapa_shared(smem_u32(rp + rank * 256 + piece * 4), dst), hv,
+                    mapa_shared(smem_u32(&mb[pass]), dst));
+      }
+      if (tid < 256) {
+        if (!mbar_wait(&mb[pass], 0)) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
         uint32_t v[kMaxCluster];
 #pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c) v[c] = c < C ? cluster.map_shared_rank(hb, c)[tid] : 0u;
+        for (int c = 0; c < kMaxCluster; ++c) v[c] = c < C ? rp[c * 256 + tid] : 0u;
         uint32_t t = 0;
 #pragma unroll
         for (int c = 0; c < kMaxCluster; ++c) t += v[c];
         tot_s[tid] = t;
+        hist[(pass + 1) & 1][tid] = 0;  // the next pass's histogram (pushed a pass ago)
       }
       __syncthreads();
       if (tid < 32) {
@@ -238,7 +286,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
       mask |= 255u << shift;
       krem = ctl[1];
       const bool whole_bin = (ctl[4] == krem);  // every key of the boundary bin is kept
-      __syncthreads();
+      // no barrier here: ctl and tot_s are next written after the next
+      // pass's first barrier
       if (whole_bin) break;  // same decision in every CTA (same cluster-wide histogram)
     }
   }
@@ -288,13 +337,24 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
       cnt[1] = incl;
     }
   }
-  cluster.sync();  // every CTA's totals are published
-  if (tid < 32) {  // lane c reads CTA c's counts; sum over the lower ranks
+  __syncthreads();
+  if (!peers_ready) {
+    cluster_wait_acquire();
+    peers_ready = true;
+  }
+  if (tid < C)  // this CTA's totals into slot `rank` of CTA tid
+    st_async_v4(mapa_shared(smem_u32(&crecv[rank]), tid),
+                make_uint4((uint32_t)cnt[0], (uint32_t)cnt[1], 0u, 0u),
+                mapa_shared(smem_u32(&mb[4]), tid));
+  // every push of this CTA is issued; the wait at the end keeps every CTA
+  // resident until all of them are
+  cluster_arrive_release();
+  if (tid < 32) {  // lane c takes CTA c's counts; sum over the lower ranks
+    if (!mbar_wait(&mb[4], 0)) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
     int gv = 0, ev = 0;
     if (lane < rank) {
-      const int* rc = cluster.map_shared_rank(cnt, lane);
-      gv = rc[0];
-      ev = rc[1];
+      gv = (int)crecv[lane].x;
+      ev = (int)crecv[lane].y;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -306,7 +366,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
       ctl[3] = ev;
     }
   }
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
+  __syncthreads();
 
   if (p.top_k > 0) {
     const int gt_before = ctl[2], eq_before = ctl[3];
@@ -360,6 +420,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
     for (int j = budget + tid; j < p.cap; j += blockDim.x) out[j] = -1;
     if (tid == 0) p.counts[(size_t)b * p.rows + row] = budget;
   }
+  cluster_wait_acquire();
+}
+
+size_t select_smem_bytes(int slice) {
+  return align_up((size_t)slice * 4, 16) + 4 * kMaxCluster * 256 * 4 + kMaxCluster * 16 + 5 * 8;
 }
 
 bool select_shape(int max_prefix, int* C, int* slice) {
@@ -458,13 +523,19 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
   p.cap = cap;
   p.rows = per_head ? num_kv_heads : 1;
   p.slice = slice;
+  // the cluster forms the keys itself when its CTAs have few loads to issue
+  // (up to kFusedLoads per CTA); otherwise the score kernel spreads them
+  p.fused = capture_mode == VG_CAPTURE_GROUP_SUM &&
+                    (long long)(per_head ? 1 : num_kv_heads) * slice <= kFusedLoads
+                ? 1
+                : 0;
 
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
     if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxSlice * 4) != cudaSuccess ||
+                             (int)select_smem_bytes(kMaxSlice)) != cudaSuccess ||
         cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess)
       return VG_ERR_LAUNCH;
@@ -479,11 +550,12 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
   scfg.stream = stream;
   scfg.attrs = pdl;
   scfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&scfg, select_score_kernel, p) != cudaSuccess) return VG_ERR_LAUNCH;
+  if (!p.fused && cudaLaunchKernelEx(&scfg, select_score_kernel, p) != cudaSuccess)
+    return VG_ERR_LAUNCH;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, p.rows, batch);
   cfg.blockDim = dim3(kSelThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)slice * 4;
+  cfg.dynamicSmemBytes = select_smem_bytes(slice);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
