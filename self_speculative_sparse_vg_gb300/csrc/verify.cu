@@ -104,7 +104,12 @@ constexpr int kMPad = 128;             // UMMA M
 // 64 columns), O (<= 128 fp32), Q as the A operand (<= 64 bf16-pair columns).
 constexpr int kTmemCols = 512;
 constexpr int kSCol = 0, kOCol = 2 * kVTile, kQCol = kOCol + 128;
-constexpr float kRescaleLog2 = 8.f;    // O, l follow a new row max only past a 2^8 growth
+// O and l follow a new row maximum only past a 2^32 growth: until then P is
+// taken relative to the older reference, so one entry of P is at most 2^32
+// (exact range in bf16 and fp32, same relative precision) and l, O stay far
+// below the fp32 range (<= 2^32 per position of a split).  A rescale must
+// wait for the last P.V, so it is kept off the common path.
+constexpr float kRescaleLog2 = 32.f;
 constexpr int kChunk = 32;             // columns a softmax pass holds in registers
 constexpr int kCapStride = kChunk + 1; // floats per staged capture row
 
@@ -115,16 +120,16 @@ struct VerifyLayout {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kCapFloats = 4 * 16 * kCapStride;  // per-warp Collect-2 staging
   static constexpr int kAllFloats = 2 * 4 * kVTile;       // Collect-All partials [slot][warp]
-  static constexpr int kBars = 12;                        // besides the ring's 2 per stage
+  static constexpr int kBars = 12;                        // besides the ring's 4 per stage
   static constexpr int kSliceMax = 1024;                  // sparse: union pages of one split
   static size_t bytes(int stages) {
     return 1024 + (size_t)stages * kStageBytes + (size_t)(kCapFloats + kAllFloats) * 4 +
-           (size_t)kSliceMax * 8 + (2 * (size_t)stages + kBars) * 8 + 16;
+           (size_t)kSliceMax * 8 + (4 * (size_t)stages + kBars) * 8 + 16;
   }
 };
 
 struct VerifyBars {
-  uint64_t *full, *empty, *s_full, *p_full, *capfull, *capfree;
+  uint64_t *kfull, *vfull, *kempty, *empty, *s_full, *p_full, *capfull, *capfree;
   int stages;
 };
 
@@ -472,14 +477,23 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   uint32_t* sl_mask = reinterpret_cast<uint32_t*>(sl_page + Lay::kSliceMax);  // union slice
   VerifyBars bars;
   bars.stages = stages;
-  bars.full = reinterpret_cast<uint64_t*>(sl_mask + Lay::kSliceMax);
-  bars.empty = bars.full + stages;    // P(t) V(t) done: ring stage, S and P buffer free
+  bars.kfull = reinterpret_cast<uint64_t*>(sl_mask + Lay::kSliceMax);  // K half landed
+  bars.vfull = bars.kfull + stages;   // V half landed
+  bars.kempty = bars.vfull + stages;  // Q K(t)^T done: K half free
+  bars.empty = bars.kempty + stages;  // P(t) V(t) done: V half, S and P buffer free
   bars.s_full = bars.empty + stages;  // S of a buffer computed (tensor-core commit)
   bars.p_full = bars.s_full + 2;      // P of a buffer written by every softmax warp
   bars.capfull = bars.p_full + 2;     // [copy][slot]: Collect-All partials written
   bars.capfree = bars.capfull + 4;    // [copy][slot]: Collect-All slot read
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars.capfree + 4);
 
+  // the K/V tensor maps are kernel parameters, independent of earlier
+  // kernels: fetch their descriptors before anything else so that the first
+  // TMA does not wait for them
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
   // programmatic dependent launch: inputs may come from the previous kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
@@ -520,9 +534,28 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
     }
   }
 
+  // Q rows of the softmax warps: loads issued now, written to tensor memory
+  // once it is allocated (lane c * RPC + m holds packed row m of copy c,
+  // every other lane zero: its logits are exactly zero)
+  uint4 qreg[HD / 8];
+  if (warp < 4) {
+    const int row = 32 * warp + lane;
+    const int cp = row / RPC, mm = row - cp * RPC;
+    const uint4* src = nullptr;
+    if (cp < CS && mm < M) {
+      int i, qi;
+      row_of(mm, g, R, i, qi);
+      src = reinterpret_cast<const uint4*>(p.q + ((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD);
+    }
+#pragma unroll
+    for (int k = 0; k < HD / 8; ++k) qreg[k] = src ? src[k] : make_uint4(0, 0, 0, 0);
+  }
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&bars.full[s], 1);
+      mbar_init(&bars.kfull[s], 1);
+      mbar_init(&bars.vfull[s], 1);
+      mbar_init(&bars.kempty[s], 1);
       mbar_init(&bars.empty[s], 1);
     }
     const int nwc = CS == 1 ? NS : 4 / CS;  // warps per copy holding rows
@@ -545,23 +578,14 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   // 2 (warps 0-3 and 5); the producer starts its loads at once
   constexpr int kQReadyBar = 2, kQReadyThreads = 5 * 32;
   if (warp < 4) {
-    // Q -> tensor memory (A operand): lane c * RPC + m holds packed row m of
-    // copy c, every other lane zero (its logits are exactly zero)
-    const int row = 32 * warp + lane;
-    const int cp = row / RPC, mm = row - cp * RPC;
+    // Q -> tensor memory (A operand)
     const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
-    const uint4* src = nullptr;
-    if (cp < CS && mm < M) {
-      int i, qi;
-      row_of(mm, g, R, i, qi);
-      src = reinterpret_cast<const uint4*>(p.q + ((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD);
-    }
 #pragma unroll
     for (int half = 0; half < HD / 64; ++half) {
       uint32_t v[32];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint4 x = src ? src[half * 8 + k] : make_uint4(0, 0, 0, 0);
+        const uint4 x = qreg[half * 8 + k];
         v[4 * k] = x.x;
         v[4 * k + 1] = x.y;
         v[4 * k + 2] = x.z;
@@ -579,52 +603,74 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------- producer
-    // The warp fetches the page ids of 4 tiles (32 ids, one per lane) in one
-    // round trip; then each lane issues one TMA box (16 positions x 64 dims
-    // of K or V) of a tile as its ring stage frees up.
+    // The K and V halves of a ring stage are filled and freed separately:
+    // K(t) once Q K(t - stages)^T is done, V(t) once P(t - stages) V is done.
+    // K is issued one tile ahead of V, so that the loads the next Q K^T
+    // waits for are not held back by the softmax of older tiles.  The warp
+    // fetches the page ids of 4 tiles (32 ids, one per lane) in one round
+    // trip; each lane issues one TMA box (16 positions x 64 dims) of a half.
     if (ntiles > 0) {
-      if (lane == 0) {
-        tma_prefetch_desc(&tmk);
-        tma_prefetch_desc(&tmv);
-      }
       const uint64_t pol = l2_policy_evict_first();
-      int my_id = p.num_pages;
-      for (int lt = 0; lt < ntiles; ++lt) {
-        if ((lt & 3) == 0) {
-          const int lt_l = lt + (lane >> 3);
+      constexpr int kHalfBoxes = kPagesPerTile * (HD / 64);  // boxes of one of K / V
+      const int pi = lane / (HD / 64), dh = lane % (HD / 64);
+      // page ids of tiles [4w, 4w + 4) for the window w of the K tile, and of
+      // the window before it (V runs one tile behind)
+      int id_cur = p.num_pages, id_prev = p.num_pages;
+      for (int kt = 0; kt <= ntiles; ++kt) {
+        const int vt = kt - 1;
+        const bool new_window = kt < ntiles && (kt & 3) == 0;
+        if (new_window) {
+          id_prev = id_cur;
+          const int lt_l = kt + (lane >> 3);
           const int slot = lt_l * kPagesPerTile + (lane & 7);
           const int lp = SP ? (slot < sl_n ? sl_page[slot] : -1)
                             : (t0 + lt_l) * kPagesPerTile + (lane & 7);
-          my_id = p.num_pages;  // out of range: TMA fills zeros
+          id_cur = p.num_pages;  // out of range: TMA fills zeros
           if (lt_l < ntiles && lp >= 0 && lp < npages_b) {
-            const int e = (lt == 0 && !SP) ? pre_id
+            const int e = (kt == 0 && !SP) ? pre_id
                                            : p.page_table[(size_t)b * p.max_pages_per_seq + lp];
             if (e >= 0 && e < p.num_pages)
-              my_id = e;
+              id_cur = e;
             else
               flag_error(p.error_flag, VG_DEVERR_PAGE);
           }
         }
-        const int st = lt % stages;
-        int go = 1;
-        if (lane == 0 && lt >= stages) go = mbar_wait(&bars.empty[st], ((lt / stages) - 1) & 1);
-        go = __shfl_sync(0xffffffffu, go, 0);
-        if (!go) {
-          if (lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-          break;
+        if (kt < ntiles) {
+          const int st = kt % stages;
+          int go = 1;
+          if (lane == 0 && kt >= stages) go = mbar_wait(&bars.kempty[st], ((kt / stages) - 1) & 1);
+          go = __shfl_sync(0xffffffffu, go, 0);
+          if (!go) {
+            if (lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+            break;
+          }
+          const int id = __shfl_sync(0xffffffffu, id_cur, (kt & 3) * 8 + (pi & 7));
+          if (lane == 0) mbar_arrive_expect_tx(&bars.kfull[st], kTileBytes);
+          __syncwarp();
+          if (lane < kHalfBoxes)
+            tma_load_4d(ring + st * kStageBytes + dh * Lay::kHalfBytes + pi * kPageSize * 128, &tmk,
+                        &bars.kfull[st], dh * 64, 0, h, id, pol);
+          __syncwarp();
         }
-        // lane -> page pi, half dh, K or V
-        constexpr int kBoxes = kPagesPerTile * (HD / 64) * 2;
-        const int pi = lane / ((HD / 64) * 2), dh = (lane >> 1) & (HD / 64 - 1), kv = lane & 1;
-        const int id = __shfl_sync(0xffffffffu, my_id, (lt & 3) * 8 + (pi & 7));
-        if (lane == 0) mbar_arrive_expect_tx(&bars.full[st], kStageBytes);
-        __syncwarp();
-        if (lane < kBoxes) {
-          uint8_t* dst = ring + st * kStageBytes + kv * kTileBytes + dh * Lay::kHalfBytes +
-                         pi * kPageSize * 128;
-          tma_load_4d(dst, kv ? &tmv : &tmk, &bars.full[st], dh * 64, 0, h, id, pol);
+        if (vt >= 0) {
+          const int st = vt % stages;
+          int go = 1;
+          if (lane == 0 && vt >= stages) go = mbar_wait(&bars.empty[st], ((vt / stages) - 1) & 1);
+          go = __shfl_sync(0xffffffffu, go, 0);
+          if (!go) {
+            if (lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+            break;
+          }
+          const int idv = new_window ? id_prev : id_cur;  // V's tile is in the window before
+          const int id = __shfl_sync(0xffffffffu, idv, (vt & 3) * 8 + (pi & 7));
+          if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[st], kTileBytes);
+          __syncwarp();
+          if (lane < kHalfBoxes)
+            tma_load_4d(ring + st * kStageBytes + kTileBytes + dh * Lay::kHalfBytes +
+                            pi * kPageSize * 128,
+                        &tmv, &bars.vfull[st], dh * 64, 0, h, id, pol);
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
   } else if (warp == kMmaWarp) {
@@ -642,7 +688,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
         bool moved = false;
         if (nq < ntiles) {
           const int st = nq % stages, sb = nq & 1;
-          if (mbar_test_wait(&bars.full[st], (nq / stages) & 1) &&
+          if (mbar_test_wait(&bars.kfull[st], (nq / stages) & 1) &&
               (nq < 2 || mbar_test_wait(&bars.empty[(nq - 2) % stages], ((nq - 2) / stages) & 1))) {
             tc_fence_after();
             const uint32_t kb = ring_u + st * kStageBytes;
@@ -653,13 +699,15 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
               umma_bf16_ts(tmem + kSCol + sb * kVTile, tmem + kQCol + ks * 8, bd, id_qk, ks > 0);
             }
             umma_commit(&bars.s_full[sb]);
+            umma_commit(&bars.kempty[st]);  // K half of the stage free for the producer
             ++nq;
             moved = true;
           }
         }
         if (np < nq) {
           const int st = np % stages, sb = np & 1;
-          if (mbar_test_wait(&bars.p_full[sb], (np >> 1) & 1)) {
+          if (mbar_test_wait(&bars.p_full[sb], (np >> 1) & 1) &&
+              mbar_test_wait(&bars.vfull[st], (np / stages) & 1)) {
             tc_fence_after();
             const uint32_t vb = ring_u + st * kStageBytes + kTileBytes;
 #pragma unroll
