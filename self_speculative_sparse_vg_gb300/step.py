@@ -36,6 +36,12 @@ class DecodeStep:
     error_flag: torch.Tensor
     num_splits: int = 0
     extra: dict = field(default_factory=dict)
+    # The step's inputs (q_verify, draft_q) and results (out_verify,
+    # out_draft; indices, counts) are views into three flat buffers, so that a
+    # host round trip of a step is one copy in and two copies out.
+    io_in: Optional[torch.Tensor] = None      # bf16: q_verify, then draft_q
+    io_out: Optional[torch.Tensor] = None     # bf16: out_verify, then out_draft
+    io_sel: Optional[torch.Tensor] = None     # int32: indices, then counts
 
     @classmethod
     def create(cls, inp: Inputs, device="cuda", capture_mode=vg.CAPTURE_GROUP_SUM,
@@ -61,16 +67,25 @@ class DecodeStep:
         wsv = vg.zero_workspace(vg.verify_workspace_bytes(B, R, Hq, Hkv, d, Lmax, num_splits), dev)
         wsd = vg.zero_workspace(vg.sparse_draft_workspace_bytes(B, Hq, Hkv, d, cap, max(k, 1)), dev)
         wss = vg.zero_workspace(vg.select_workspace_bytes(B, Hkv, Lmax, per_head), dev)
-        return cls(spec=s, device=dev, kv=kv, q_verify=inp.q_verify.to(dev),
-                   draft_q=inp.draft_q.to(dev), prefix_lens=prefix, capture_mode=capture_mode,
-                   per_head=per_head, capture=capture,
-                   out_verify=torch.zeros(B, R, Hq, d, dtype=torch.bfloat16, device=dev),
-                   indices=torch.full((B, rows, cap), -7, dtype=torch.int32, device=dev),
-                   counts=torch.zeros(B, rows, dtype=torch.int32, device=dev),
-                   out_draft=torch.zeros(max(k, 1), B, Hq, d, dtype=torch.bfloat16, device=dev),
+        nv, nd = B * R * Hq * d, max(k, 1) * B * Hq * d
+        io_in = torch.zeros(nv + nd, dtype=torch.bfloat16, device=dev)
+        q_verify = io_in[:nv].view(B, R, Hq, d)
+        draft_q = io_in[nv:].view(max(k, 1), B, Hq, d)
+        q_verify.copy_(inp.q_verify)
+        draft_q[:k].copy_(inp.draft_q)
+        io_out = torch.zeros(nv + nd, dtype=torch.bfloat16, device=dev)
+        ni = B * rows * cap
+        io_sel = torch.zeros(ni + B * rows, dtype=torch.int32, device=dev)
+        indices = io_sel[:ni].view(B, rows, cap)
+        indices.fill_(-7)
+        return cls(spec=s, device=dev, kv=kv, q_verify=q_verify, draft_q=draft_q[:k] if k else draft_q[:0],
+                   prefix_lens=prefix, capture_mode=capture_mode, per_head=per_head,
+                   capture=capture, out_verify=io_out[:nv].view(B, R, Hq, d),
+                   indices=indices, counts=io_sel[ni:].view(B, rows),
+                   out_draft=io_out[nv:].view(max(k, 1), B, Hq, d),
                    tail_start=prefix.clone(), cur_len=cur.contiguous(), ws_verify=wsv,
                    ws_draft=wsd, ws_select=wss, error_flag=torch.zeros(1, dtype=torch.int32, device=dev),
-                   num_splits=num_splits)
+                   num_splits=num_splits, io_in=io_in, io_out=io_out, io_sel=io_sel)
 
     @property
     def max_tail(self):
