@@ -212,9 +212,13 @@ vg_status vg_sparse_verify_attention(const vg_paged_kv* kv, const void* q,
  *   indices  int32 [batch][rows][cap], ascending, entries past the count = -1.
  *   counts   int32 [batch][rows].
  *   cap      >= min(max_prefix, n_sink + n_recent + top_k).
- *   workspace  vg_select_workspace_bytes() bytes: the positions' score keys
- *            (one 4-byte key per prefix position and selection row).
- * The call launches a score kernel and a cluster selection kernel on `stream`.
+ *   workspace  vg_select_workspace_bytes() bytes: room for the positions'
+ *            score keys (one 4-byte key per prefix position and selection
+ *            row); no initialisation needed.
+ * The call launches one thread-block-cluster selection kernel on `stream`,
+ * preceded by a score kernel that writes the keys to the workspace when the
+ * cluster would have many capture loads per CTA (long prefixes, raw-row and
+ * attention-weight captures).
  * Supported: max_prefix <= 262144, num_q_heads / num_kv_heads <= 8.
  * ------------------------------------------------------------------------- */
 size_t vg_select_workspace_bytes(int batch, int num_kv_heads, int max_prefix, int per_head);
