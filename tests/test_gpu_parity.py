@@ -231,6 +231,24 @@ def test_draft_graph_replay_eager_and_empty_list(kw):
     assert (st.out_draft[0].float() == 0).all()
 
 
+@pytest.mark.parametrize("kw", [
+    dict(top_k=0, n_sink=4, n_recent=16),                 # no radix pass: sink and recent only
+    dict(top_k=50, n_sink=0, n_recent=0),                 # pure top-k
+    dict(top_k=1, n_sink=0, n_recent=1),
+    # lengths on both sides of the cluster slices (4 CTAs of 1250 positions)
+    dict(prefix_lens=(1249, 1250, 1251, 3999, 5000), batch=5, top_k=300, n_sink=3, n_recent=7),
+    dict(prefix_lens=(20000,), batch=1, top_k=19000, n_sink=4, n_recent=64),  # nearly all kept
+], ids=["top0", "pure_topk", "top1", "slice_edges", "nearly_all"])
+@pytest.mark.parametrize("mode,per_head", [(1, False), (1, True), (2, False)])
+def test_select_edge_cases(kw, mode, per_head):
+    """The selector against the oracle's fp32 mirror on a generator-made
+    capture with many exact ties: bit-exact index sets at the edges of its
+    parameters and of the cluster's slices."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    P.check_select_synthetic(small_spec(**kw), mode, per_head)
+
+
 def test_device_errors_flag_and_skip():
     """Bad page ids, indices, counts and lengths set the error flag; the
     offending load is skipped (no fault)."""

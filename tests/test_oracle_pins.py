@@ -441,3 +441,16 @@ def test_sparse_verify_equals_masked_textbook_attention():
             mask[allowed] = 0.0
             w = sp_softmax(S + mask)
             np.testing.assert_allclose(got[0, i, h], w @ v[0][0], rtol=0, atol=1e-12)
+
+
+def test_select_without_top_k_is_sink_and_recent():
+    """top_k = 0 keeps exactly [0, n_sink) and [L - n_recent, L), whatever the
+    scores; with n_sink = n_recent = 0 the set is the top_k by a plain stable
+    sort (score descending, position ascending)."""
+    rng = np.random.default_rng(3)
+    L = 300
+    score = np.round(rng.standard_normal(L), 1)  # many exact ties
+    got = O.select_row(score, L, 0, 5, 7)
+    assert got.tolist() == list(range(5)) + list(range(L - 7, L))
+    order = sorted(range(L), key=lambda j: (-score[j], j))[:40]
+    assert O.select_row(score, L, 40, 0, 0).tolist() == sorted(order)
