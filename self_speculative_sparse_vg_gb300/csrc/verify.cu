@@ -881,7 +881,7 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
     const int sms = device_sm_count();
     int splits = std::max(1, sms / pairs);
     tps = ceil_div(tiles, splits);
-    if (batch > 1) tps = std::min(tps, 16);  // ragged lengths: small chunks balance SMs
+    if (batch > 1) tps = std::min(tps, 24);  // ragged lengths: chunks small enough to balance SMs
     tps = std::max(tps, std::min(tiles, 2));
   }
   if (ceil_div(tiles, tps) > kMaxSplits) tps = ceil_div(tiles, kMaxSplits);
