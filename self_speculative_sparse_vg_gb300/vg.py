@@ -274,5 +274,7 @@ def sparse_draft_attention(kv: PagedKV, q, indices, counts, per_head, tail_start
 
 
 def zero_workspace(nbytes: int, device) -> torch.Tensor:
-    """A zero-filled byte workspace (the counters inside must start at zero)."""
+    """A zero-filled byte workspace.  No call needs its workspace initialised
+    (every partial is written before it is read); zeros only keep a fresh
+    buffer free of stale bytes."""
     return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
