@@ -365,7 +365,10 @@ __device__ __forceinline__ float safe_ref(float m) { return m == -INFINITY ? 0.f
 // the merged row goes to dst[0 .. HD) as bf16.
 // Thread t owns float4 column t % (HD / 4) for splits t / (HD / 4) + k * G;
 // every split's loads are issued before any is used (one round trip for
-// S <= G * kMergePer), then the G split groups are reduced in shared memory.
+// S <= G * kMergePer).  Warp 0 forms the batch maximum, weights and
+// normaliser from the (m, l) pairs with shuffles and publishes them behind
+// one barrier; the G split groups are then reduced in shared memory behind
+// one more.
 constexpr int kMergeThreads = 256;
 constexpr int kMergePer = 8;
 
@@ -378,13 +381,15 @@ __device__ __forceinline__ void merge_splits(const float* o_base, size_t o_strid
                                              float* lse = nullptr) {
   constexpr int COLS = HD / 4;
   constexpr int G = kMergeThreads / COLS;
-  const int t = threadIdx.x, col = t % COLS, grp = t / COLS;
-  float* red = smem_f;                                         // [8]
-  float* w_s = smem_f + 8;                                     // [G * kMergePer] of a batch
+  constexpr int NB = G * kMergePer;   // splits per batch (<= 128)
+  constexpr int LP = NB / 32;         // (m, l) pairs per lane of warp 0
+  const int t = threadIdx.x, lane = t & 31, col = t % COLS, grp = t / COLS;
+  float* red = smem_f;                                         // [8]: m_new, corr, l of the batch
+  float* w_s = smem_f + 8;                                     // [NB] weights of a batch
   float4* part = reinterpret_cast<float4*>(smem_f + 8 + 128);  // [G][COLS]
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float mx_all = -INFINITY, lt_all = 0.f;
-  for (int s0 = 0; s0 < S; s0 += G * kMergePer) {
+  for (int s0 = 0; s0 < S; s0 += NB) {
     float4 v[kMergePer];
 #pragma unroll
     for (int k = 0; k < kMergePer; ++k) {
@@ -392,52 +397,55 @@ __device__ __forceinline__ void merge_splits(const float* o_base, size_t o_strid
       v[k] = s < S ? __ldcg(reinterpret_cast<const float4*>(o_base + (size_t)s * o_stride) + col)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    // (m, l) of this batch's splits: thread t < batch size loads one pair
-    const int nb = min(S - s0, G * kMergePer);
-    float m_t = -INFINITY, l_t = 0.f;
-    if (t < nb) {
-      m_t = __ldcg(ml_base + (size_t)(s0 + t) * ml_stride);
-      l_t = __ldcg(ml_base + (size_t)(s0 + t) * ml_stride + 1);
+    // warp 0 forms the batch maximum, the weights and the normaliser from all
+    // the batch's (m, l) pairs (shuffles), then one barrier publishes them
+    if (t < 32) {
+      float mw[LP], lw[LP];
+#pragma unroll
+      for (int i = 0; i < LP; ++i) {
+        const int s = s0 + lane + 32 * i;
+        mw[i] = s < S ? __ldcg(ml_base + (size_t)s * ml_stride) : -INFINITY;
+        lw[i] = s < S ? __ldcg(ml_base + (size_t)s * ml_stride + 1) : 0.f;
+      }
+      float mb = mw[0];
+#pragma unroll
+      for (int i = 1; i < LP; ++i) mb = fmaxf(mb, mw[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+      const float m_new = fmaxf(mx_all, mb);
+      const float ref = safe_ref(m_new);
+      float lb = 0.f;
+#pragma unroll
+      for (int i = 0; i < LP; ++i) {
+        const float w = ex2(mw[i] - ref);  // 0 past S (m = -inf)
+        w_s[lane + 32 * i] = w;
+        lb += w * lw[i];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
+      if (lane == 0) {
+        red[0] = m_new;
+        red[1] = ex2(mx_all - ref);
+        red[2] = lb;
+      }
     }
-    float mw = m_t;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
     __syncthreads();
-    if ((t & 31) == 0) red[t >> 5] = mw;
-    __syncthreads();
-    float mb = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) mb = fmaxf(mb, red[w]);
-    const float m_new = fmaxf(mx_all, mb);
-    const float ref = safe_ref(m_new);
-    const float corr = ex2(mx_all - ref);
-    if (t < nb) w_s[t] = ex2(m_t - ref);
-    float lw = t < nb ? ex2(m_t - ref) * l_t : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-    __syncthreads();
-    if ((t & 31) == 0) red[t >> 5] = lw;
-    __syncthreads();
-    float lb = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) lb += red[w];
-    lt_all = lt_all * corr + lb;
-    mx_all = m_new;
+    const float corr = red[1];
+    lt_all = lt_all * corr + red[2];
+    mx_all = red[0];
     acc.x *= corr;
     acc.y *= corr;
     acc.z *= corr;
     acc.w *= corr;
 #pragma unroll
     for (int k = 0; k < kMergePer; ++k) {
-      const int s = s0 + grp + k * G;
-      if (s < S) {
-        const float w = w_s[grp + k * G];
-        acc.x += w * v[k].x;
-        acc.y += w * v[k].y;
-        acc.z += w * v[k].z;
-        acc.w += w * v[k].w;
-      }
+      const float w = w_s[grp + k * G];
+      acc.x += w * v[k].x;
+      acc.y += w * v[k].y;
+      acc.z += w * v[k].z;
+      acc.w += w * v[k].w;
     }
+    if (s0 + NB < S) __syncthreads();  // w_s and red are rewritten by the next batch
   }
   part[grp * COLS + col] = acc;
   __syncthreads();
