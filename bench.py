@@ -215,18 +215,83 @@ print(json.dumps({{"step_s": min(times), "reps": len(times)}}))
                       f"selection, {reps} rep(s), best), single thread, float64 numpy"}
 
 
+REFERENCE_BUDGET_S = 150.0  # wall time of the whole reference arm (warm-up + timed steps)
+
+_REFERENCE_CODE = """
+import sys, time, json
+sys.path.insert(0, {root!r})
+import numpy as np
+from oracle import vg_oracle as O
+from self_speculative_sparse_vg_gb300.workloads import WORKLOADS, make_inputs
+s = WORKLOADS[{workload!r}]
+inp = make_inputs(s)
+B, Hkv, g = s.batch, s.num_kv_heads, s.group
+q = inp.q_verify.double().numpy()
+k = [x.double().numpy() for x in inp.k_dense]
+v = [x.double().numpy() for x in inp.v_dense]
+dq = inp.draft_q.double().numpy()
+units = [(b, h) for b in range(B) for h in range(Hkv)]       # (sequence, KV head)
+weight = [s.prefix_lens[b] + s.n_rows for b, h in units]     # oracle cost grows with the length
+
+
+def run(sel_units):
+    # verify of the units' query heads over the whole prefix, their selection
+    # (one row per unit), and the k draft steps: the oracle's code as it stands
+    t0 = time.perf_counter()
+    for b, h in sel_units:
+        qs = q[b:b + 1, :, h * g:(h + 1) * g]
+        ks, vs = [k[b][h:h + 1]], [v[b][h:h + 1]]
+        lens = [s.prefix_lens[b]]
+        out, rows = O.verify_attention(qs, ks, vs, lens, s.softmax_scale)
+        sel = O.select_kv(O.group_sum(rows, 1), O.CAPTURE_GROUP_SUM, lens, g, 1, s.top_k,
+                          s.n_sink, s.n_recent, False)
+        for t in range(1, s.n_drafts + 1):
+            O.sparse_draft_attention(dq[t - 1][b:b + 1, h * g:(h + 1) * g], ks, vs, sel, False,
+                                     lens, [lens[0] + t], s.softmax_scale)
+    return time.perf_counter() - t0
+
+
+n_steps = {n_steps}
+t_unit = run(units[:1]) / weight[0]                           # calibration (not reported)
+per_step = max(1, min(len(units), int({budget} / (n_steps * t_unit * max(weight)))))
+times, i = [], 0
+for _ in range(n_steps):
+    sel_units = [units[(i + j) % len(units)] for j in range(per_step)]
+    i += per_step
+    w = sum(weight[units.index(u)] for u in sel_units)
+    times.append(run(sel_units) * sum(weight) / w * 1e6)
+print(json.dumps({{"step_us": times, "units_per_step": per_step, "units": len(units)}}))
+"""
+
+
 def run_reference(args, rank, world):
+    """The float64 oracle as it stands, timed on the host cores (one thread),
+    on the workload of `--workload`.  Each step runs a bounded sample of the
+    decode step -- `units_per_step` of the (sequence, KV head) units, each a
+    verify of its query heads over the full prefix, its selection and the k
+    draft steps -- scaled to a full step by the units' prefix lengths, so that
+    warm-up plus timed steps end within REFERENCE_BUDGET_S; with few steps
+    every step is a full decode step.  Under torchrun rank 0 alone runs."""
     if rank != 0:
         return
     from self_speculative_sparse_vg_gb300.workloads import WORKLOADS
     spec = WORKLOADS[args.workload]
-    steps = []
-    for _ in range(args.warmup + args.steps):
-        steps.append(cpu_baseline(args.workload)["value"])
-    timed = steps[args.warmup:]
+    n = args.warmup + args.steps
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = _REFERENCE_CODE.format(root=ROOT, workload=args.workload, n_steps=n,
+                                  budget=REFERENCE_BUDGET_S)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    timed = res["step_us"][args.warmup:]
     val = statistics.mean(timed)
-    cb = {"value": val, "unit": "us", "cores": 1, "kind": "oracle",
-          "sample": f"each step one full decode step of {args.workload}, single thread"}
+    sample = (f"each step {res['units_per_step']} of the {res['units']} (sequence, KV head) units "
+              f"of one {args.workload} decode step (verify of the unit's query heads over its "
+              f"prefix, its selection, {spec.n_drafts} draft steps), scaled to the full step by "
+              f"prefix length; single thread")
+    cb = {"value": val, "unit": "us", "cores": 1, "kind": "oracle", "sample": sample}
     print(json.dumps({"impl": "reference", "metric": METRIC, "value": val, "unit": "us",
                       "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                       "ms_per_step": val / 1e3, "higher_is_better": False, "scaling": "weak",
