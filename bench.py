@@ -2,17 +2,31 @@
 
 One step = 1 verification attention (k+1 rows, Collect-2 capture) + 1 KV
 selection + k sparse draft attentions, on one seeded synthetic GQA layer.
+The headline workload is the batch-8 Llama-3-8B-shaped layer with contexts
+drawn in [16K, 64K]; the 32K and 128K single-sequence layers are measured in
+the same run and reported under "workloads".
 
-Timing: CUDA events on the launching stream around each kernel.  The L2 is
-flushed before the verify call and before every draft call, as other layers
-would evict it in a real model: between steps a buffer larger than L2 is
-written and then another one is read; before each draft call one is read.
-Reading last leaves L2 holding clean, unrelated lines, so a timed kernel does
-not pay for write-backs of the flush's own dirty data.  The flushes are
-outside the timed segments.  value = mean over K steps of the summed segments.
+Cold L2 for every step kernel, as in a real model where other layers evict
+it: before the verify call a buffer larger than L2 is written and another is
+read, and before each draft call one is read (reading last leaves L2 holding
+clean, unrelated lines, so a timed kernel does not pay for write-backs of the
+flush's own dirty data).
+
+Two device timings (CUDA events on the launching stream):
+  value       the step as it runs in a stream: the whole cold step (flushes
+              and step kernels) is captured once as a CUDA graph and
+              replayed K times, and the same graph with the step kernels left
+              out (flushes only) is replayed K times; value = mean time per
+              replay of the first minus that of the second.  Stage figures
+              ("stages_graph_us") are the full graph minus the graph without
+              that stage.
+  stages_us   every call of K eagerly launched cold steps bracketed by its
+              own event pair; their sum is "events_us_per_step".  An event
+              pair around a call adds its own ~2 us, so this is an upper
+              bound; the verify segment is the roofline's kernel time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference]
+                  [--impl ours|reference] [--no-cpu-baseline] [--no-extra]
 
 Under torchrun each rank runs an independent replica on its own GPU (the path
 shards by sequence with no exchange); the max over ranks is reported.
@@ -27,12 +41,12 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "llama8b_32k"
+DEFAULT_WORKLOAD = "llama8b_b8_16k_64k"
+EXTRA_WORKLOADS = ("llama8b_32k", "qwen14b_128k")
 METRIC = "us_per_decode_step"
 METRIC_DESC = "µs per decode step (verify+select+sparse draft) and HBM GB/s vs peak"
 
@@ -131,7 +145,7 @@ def verify_traffic(workload):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    """nvidia-smi clock / throttle-reason samples while the GPU works."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -174,52 +188,23 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "reasons": sorted(reasons),
+                "window": "every GPU phase of the run: warm-up, timed steps, studies, "
+                          "the other workloads"}
 
 
-def cpu_baseline(workload, reps=1):
-    """Time the float64 oracle (as it stands) on one full decode step of the
-    workload, single-threaded, in a fresh process."""
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = f"""
-import sys, time, json
-sys.path.insert(0, {ROOT!r})
-import numpy as np
-from oracle import vg_oracle as O
-from self_speculative_sparse_vg_gb300.workloads import WORKLOADS, make_inputs
-s = WORKLOADS[{workload!r}]
-inp = make_inputs(s)
-q = inp.q_verify.double().numpy()
-k = [x.double().numpy() for x in inp.k_dense]
-v = [x.double().numpy() for x in inp.v_dense]
-dq = inp.draft_q.double().numpy()
-times = []
-for _ in range({reps}):
-    t0 = time.perf_counter()
-    out, rows = O.verify_attention(q, k, v, s.prefix_lens, s.softmax_scale)
-    sel = O.select_kv(O.group_sum(rows, s.num_kv_heads), O.CAPTURE_GROUP_SUM, s.prefix_lens,
-                      s.num_q_heads, s.num_kv_heads, s.top_k, s.n_sink, s.n_recent, s.per_head)
-    for t in range(1, s.n_drafts + 1):
-        O.sparse_draft_attention(dq[t - 1], k, v, sel, s.per_head, s.prefix_lens,
-                                 [L + t for L in s.prefix_lens], s.softmax_scale)
-    times.append(time.perf_counter() - t0)
-print(json.dumps({{"step_s": min(times), "reps": len(times)}}))
-"""
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       timeout=1800)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr[-2000:])
-    res = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": res["step_s"] * 1e6, "unit": "us", "cores": 1, "kind": "oracle",
-            "sample": f"one full decode step of {workload} (verify all heads and rows, float64 "
-                      f"selection, {reps} rep(s), best), single thread, float64 numpy"}
-
-
-REFERENCE_BUDGET_S = 150.0  # wall time of the whole reference arm (warm-up + timed steps)
-
-_REFERENCE_CODE = """
-import sys, time, json
+# ----------------------------------------------------------------- oracle arm
+# The float64 oracle, as it stands, on one decode step of a workload: per
+# (sequence, KV head) unit, the verify of the unit's query heads over its
+# prefix, its selection and the k draft steps.  Run in a fresh process
+# without CUDA; with several cores the units are spread over a fork pool (one
+# BLAS thread per worker).  A step times all units, or a sample of them when
+# a full step does not fit the budget, scaled to the full step by the units'
+# prefix lengths (the oracle's cost grows with the length).
+_ORACLE_CODE = """
+import sys, os, time, json
 sys.path.insert(0, {root!r})
+import multiprocessing as mp
 import numpy as np
 from oracle import vg_oracle as O
 from self_speculative_sparse_vg_gb300.workloads import WORKLOADS, make_inputs
@@ -230,68 +215,122 @@ q = inp.q_verify.double().numpy()
 k = [x.double().numpy() for x in inp.k_dense]
 v = [x.double().numpy() for x in inp.v_dense]
 dq = inp.draft_q.double().numpy()
-units = [(b, h) for b in range(B) for h in range(Hkv)]       # (sequence, KV head)
-weight = [s.prefix_lens[b] + s.n_rows for b, h in units]     # oracle cost grows with the length
+del inp
+units = [(b, h) for b in range(B) for h in range(Hkv)]
+weight = [s.prefix_lens[b] + s.n_rows for b, h in units]
 
 
-def run(sel_units):
-    # verify of the units' query heads over the whole prefix, their selection
-    # (one row per unit), and the k draft steps: the oracle's code as it stands
-    t0 = time.perf_counter()
-    for b, h in sel_units:
-        qs = q[b:b + 1, :, h * g:(h + 1) * g]
-        ks, vs = [k[b][h:h + 1]], [v[b][h:h + 1]]
-        lens = [s.prefix_lens[b]]
-        out, rows = O.verify_attention(qs, ks, vs, lens, s.softmax_scale)
-        sel = O.select_kv(O.group_sum(rows, 1), O.CAPTURE_GROUP_SUM, lens, g, 1, s.top_k,
-                          s.n_sink, s.n_recent, False)
-        for t in range(1, s.n_drafts + 1):
-            O.sparse_draft_attention(dq[t - 1][b:b + 1, h * g:(h + 1) * g], ks, vs, sel, False,
-                                     lens, [lens[0] + t], s.softmax_scale)
-    return time.perf_counter() - t0
+def unit(i):
+    b, h = units[i]
+    qs = q[b:b + 1, :, h * g:(h + 1) * g]
+    ks, vs = [k[b][h:h + 1]], [v[b][h:h + 1]]
+    lens = [s.prefix_lens[b]]
+    out, rows = O.verify_attention(qs, ks, vs, lens, s.softmax_scale)
+    sel = O.select_kv(O.group_sum(rows, 1), O.CAPTURE_GROUP_SUM, lens, g, 1, s.top_k,
+                      s.n_sink, s.n_recent, False)
+    for t in range(1, s.n_drafts + 1):
+        O.sparse_draft_attention(dq[t - 1][b:b + 1, h * g:(h + 1) * g], ks, vs, sel, False,
+                                 lens, [lens[0] + t], s.softmax_scale)
+    return i
 
 
-n_steps = {n_steps}
-t_unit = run(units[:1]) / weight[0]                           # calibration (not reported)
-per_step = max(1, min(len(units), int({budget} / (n_steps * t_unit * max(weight)))))
-times, i = [], 0
+cores = {cores} or len(os.sched_getaffinity(0))
+n_steps, budget = {n_steps}, {budget}
+t0 = time.perf_counter()
+unit(0)                                                   # calibration (not reported)
+t_w = (time.perf_counter() - t0) / weight[0]
+full = t_w * sum(weight) / cores                          # estimated wall time of a step
+per_step = len(units)
+if full * n_steps > budget:                               # a sample of the units per step
+    per_step = max(1, int(len(units) * budget / (n_steps * full)))
+    per_step = max(min(cores, len(units)), per_step // cores * cores)
+pool = mp.get_context("fork").Pool(cores) if cores > 1 else None
+times, nxt = [], 0
 for _ in range(n_steps):
-    sel_units = [units[(i + j) % len(units)] for j in range(per_step)]
-    i += per_step
-    w = sum(weight[units.index(u)] for u in sel_units)
-    times.append(run(sel_units) * sum(weight) / w * 1e6)
-print(json.dumps({{"step_us": times, "units_per_step": per_step, "units": len(units)}}))
+    sel = [(nxt + j) % len(units) for j in range(per_step)]
+    nxt += per_step
+    t0 = time.perf_counter()
+    if pool is None:
+        for i in sel:
+            unit(i)
+    else:
+        pool.map(unit, sel, chunksize=1)
+    wall = time.perf_counter() - t0
+    times.append(wall * sum(weight) / sum(weight[i] for i in sel) * 1e6)
+if pool is not None:
+    pool.close()
+print(json.dumps({{"step_us": times, "units_per_step": per_step, "units": len(units),
+                  "cores": cores}}))
 """
 
 
+def host_info():
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"cpu_model": model, "nproc": len(os.sched_getaffinity(0)),
+            "machine": os.uname().machine}
+
+
+def time_oracle(workload, n_steps, cores, budget_s):
+    """Run the oracle timing in a fresh process; cores 0 = all of them."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = _ORACLE_CODE.format(root=ROOT, workload=workload, n_steps=n_steps, cores=cores,
+                               budget=budget_s)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _sample_text(res, workload, spec, n_steps):
+    part = ("every (sequence, KV head) unit" if res["units_per_step"] == res["units"] else
+            f"{res['units_per_step']} of the {res['units']} (sequence, KV head) units, scaled "
+            f"to the full step by prefix length")
+    return (f"{n_steps} step(s) of {workload}, each {part}: verify of the unit's query heads "
+            f"over its prefix, its selection, {spec.n_drafts} draft steps; float64 numpy, "
+            f"{res['cores']} worker process(es) of one thread")
+
+
+def cpu_baseline(workload):
+    """The float64 oracle (as it stands) on one decode step of the workload:
+    on all of the host's cores (the reported figure) and on one thread."""
+    from self_speculative_sparse_vg_gb300.workloads import WORKLOADS
+    spec = WORKLOADS[workload]
+    par = time_oracle(workload, 1, 0, 30.0)
+    one = time_oracle(workload, 1, 1, 30.0)
+    return {"value": par["step_us"][0], "unit": "us", "cores": par["cores"], "kind": "oracle",
+            "sample": _sample_text(par, workload, spec, 1),
+            "single_thread": {"value": one["step_us"][0], "unit": "us", "cores": 1,
+                              "sample": _sample_text(one, workload, spec, 1)},
+            "host": host_info()}
+
+
+REFERENCE_BUDGET_S = 150.0  # wall time of the timed oracle steps of the reference arm
+
+
 def run_reference(args, rank, world):
-    """The float64 oracle as it stands, timed on the host cores (one thread),
-    on the workload of `--workload`.  Each step runs a bounded sample of the
-    decode step -- `units_per_step` of the (sequence, KV head) units, each a
-    verify of its query heads over the full prefix, its selection and the k
-    draft steps -- scaled to a full step by the units' prefix lengths, so that
-    warm-up plus timed steps end within REFERENCE_BUDGET_S; with few steps
-    every step is a full decode step.  Under torchrun rank 0 alone runs."""
+    """The float64 oracle as it stands, timed on the host's cores (a fork pool
+    over the (sequence, KV head) units), on the workload of `--workload`.
+    Each of the warm-up + timed steps is a full decode step, or a bounded
+    sample of its units scaled to the full step when the run would not end
+    within REFERENCE_BUDGET_S.  Under torchrun rank 0 alone runs."""
     if rank != 0:
         return
     from self_speculative_sparse_vg_gb300.workloads import WORKLOADS
     spec = WORKLOADS[args.workload]
     n = args.warmup + args.steps
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = _REFERENCE_CODE.format(root=ROOT, workload=args.workload, n_steps=n,
-                                  budget=REFERENCE_BUDGET_S)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       timeout=3600)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr[-2000:])
-    res = json.loads(r.stdout.strip().splitlines()[-1])
-    timed = res["step_us"][args.warmup:]
-    val = statistics.mean(timed)
-    sample = (f"each step {res['units_per_step']} of the {res['units']} (sequence, KV head) units "
-              f"of one {args.workload} decode step (verify of the unit's query heads over its "
-              f"prefix, its selection, {spec.n_drafts} draft steps), scaled to the full step by "
-              f"prefix length; single thread")
-    cb = {"value": val, "unit": "us", "cores": 1, "kind": "oracle", "sample": sample}
+    res = time_oracle(args.workload, n, 0, REFERENCE_BUDGET_S)
+    val = statistics.mean(res["step_us"][args.warmup:])
+    cb = {"value": val, "unit": "us", "cores": res["cores"], "kind": "oracle",
+          "sample": _sample_text(res, args.workload, spec, n), "host": host_info()}
     print(json.dumps({"impl": "reference", "metric": METRIC, "value": val, "unit": "us",
                       "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                       "ms_per_step": val / 1e3, "higher_is_better": False, "scaling": "weak",
@@ -314,11 +353,11 @@ def run_stack(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     st = DecodeStack(spec, dev)
+    sampler = ClockSampler(local) if rank == 0 else None
     st.seed_selection()
     for _ in range(args.warmup):
         st.step()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local) if rank == 0 else None
     iters, nbytes = [], []
     kv_row = spec.num_kv_heads * spec.head_dim * 2 * 2
     R, k = spec.n_drafts + 1, spec.n_drafts
@@ -357,7 +396,7 @@ def run_stack(args, rank, world, local):
         "stages_us": {key: statistics.mean(t[key] for t in iters) for key in iters[0]},
         "algorithmic_bytes_per_iteration": statistics.mean(nbytes),
         "hbm_gbs": gbs, "hbm_frac": gbs / peak, "peak_kind": peak_kind,
-        "gpu_launches": args.steps * spec.layers * (2 * k + 3 + 1),
+        "gpu_launches": args.steps * spec.layers * st.launches_per_iteration(),
         "clocks": clocks}))
 
 
@@ -373,14 +412,168 @@ def _config(spec, n):
             "replicas": n}
 
 
+# ------------------------------------------------------------------ GPU arm
+class Flusher:
+    """Buffers larger than L2: a write then a read before a step, a read
+    before each draft step."""
+
+    def __init__(self, dev):
+        import torch
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.w = torch.empty(int(1.5 * l2), dtype=torch.uint8, device=dev)
+        self.r = torch.ones(int(1.5 * l2) // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def read(self):
+        import torch
+        torch.sum(self.r, dim=0, out=self.out)
+
+    def full(self, i=1):
+        self.w.fill_(i & 0xFF)
+        self.read()
+
+
+def _events(n):
+    import torch
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def cold_graphs(st, fl, dev):
+    """CUDA graphs of one cold step and of its variants: "full" (flushes and
+    every step kernel), "flush" (flushes only), and "no_verify",
+    "no_select", "no_drafts" (one stage left out; the kernels left in read
+    what the previous replays wrote, which is the same data)."""
+    import torch
+    k = st.spec.n_drafts
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    graphs = {}
+
+    def body(skip):
+        fl.full(1)
+        if skip not in ("verify", "all"):
+            st.verify(side)
+        if skip not in ("select", "all"):
+            st.select(side)
+        for t in range(1, k + 1):
+            fl.read()
+            if skip not in ("drafts", "all"):
+                st.draft(t, side)
+
+    with torch.cuda.stream(side):
+        body(None)  # bind the side stream's call arguments outside capture
+        torch.cuda.synchronize()
+        for name, skip in (("full", None), ("flush", "all"), ("no_verify", "verify"),
+                           ("no_select", "select"), ("no_drafts", "drafts")):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                body(skip)
+            graphs[name] = g
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    return graphs
+
+
+def time_graph(g, reps, barrier):
+    """Mean µs per replay of `reps` replays (3 untimed first), an event pair
+    around each replay on the current stream."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        g.replay()
+    barrier()
+    marks = []
+    for _ in range(reps):
+        a, b = _events(2)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        marks.append((a, b))
+    barrier()
+    return statistics.mean(a.elapsed_time(b) * 1e3 for a, b in marks)
+
+
+def measure(spec, inp, st, fl, steps, warmup, barrier, dev):
+    """Cold-step timings of one workload: the graph figure and the
+    per-call event figures."""
+    import torch
+    k = spec.n_drafts
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        fl.full(i)
+        st.run()
+    barrier()
+    graphs = cold_graphs(st, fl, dev)
+    T = {}
+    for name in ("full", "flush", "no_verify", "no_select", "no_drafts"):
+        T[name] = time_graph(graphs[name], steps, barrier)
+    del graphs
+    # every call with its own event pair
+    marks = []
+    for i in range(steps):
+        fl.full(i)
+        e = _events(3 + 2 * k)
+        e[0].record(stream)
+        st.verify()
+        e[1].record(stream)
+        st.select()
+        e[2].record(stream)
+        for t in range(1, k + 1):
+            fl.read()
+            e[1 + 2 * t].record(stream)
+            st.draft(t)
+            e[2 + 2 * t].record(stream)
+        marks.append(e)
+    barrier()
+    assert int(st.error_flag.item()) == 0, "device error flag set"
+    ver = statistics.mean(m[0].elapsed_time(m[1]) * 1e3 for m in marks)
+    sel = statistics.mean(m[1].elapsed_time(m[2]) * 1e3 for m in marks)
+    dra = statistics.mean(sum(m[1 + 2 * t].elapsed_time(m[2 + 2 * t]) * 1e3
+                              for t in range(1, k + 1)) for m in marks)
+    return {"graph_full_us": T["full"], "graph_flush_us": T["flush"],
+            "value": T["full"] - T["flush"],
+            "stages_graph_us": {"verify": T["full"] - T["no_verify"],
+                                "select": T["full"] - T["no_select"],
+                                "drafts_total": T["full"] - T["no_drafts"],
+                                "draft_each": (T["full"] - T["no_drafts"]) / max(k, 1)},
+            "stages_us": {"verify": ver, "select": sel, "drafts_total": dra,
+                          "draft_each": dra / max(k, 1)},
+            "events_us_per_step": ver + sel + dra}
+
+
+def summarize(spec, m, peak, peak_kind, launches):
+    nb = algorithmic_bytes(spec)
+    v = m["value"]
+    achieved = nb["verify"] / (m["stages_us"]["verify"] * 1e-6) / 1e9
+    return {
+        "value": v,
+        "hbm_gbs_step": nb["step"] / (v * 1e-6) / 1e9,
+        "hbm_frac_step": nb["step"] / (v * 1e-6) / 1e9 / peak,
+        "gap_to_0.70_us": v - nb["step"] / (0.70 * peak * 1e9) * 1e6,
+        "graph_full_us": m["graph_full_us"], "graph_flush_us": m["graph_flush_us"],
+        "stages_graph_us": m["stages_graph_us"],
+        "stages_us": m["stages_us"],
+        "events_us_per_step": m["events_us_per_step"],
+        "hbm_frac_step_events": nb["step"] / (m["events_us_per_step"] * 1e-6) / 1e9 / peak,
+        "stages_bytes": nb,
+        "launches_per_step": launches,
+        "roofline": {"kernel": "verify_kernel (+ split merge)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": verify_traffic(spec.name),
+                     "time": "mean event time of the verify call (cold L2) over the timed steps"},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     args = ap.parse_args()
     assert args.warmup >= 3
 
@@ -414,84 +607,39 @@ def main():
         torch.cuda.synchronize()
 
     spec = WORKLOADS[args.workload]
-    inp = make_inputs(spec)
-    st = DecodeStep.create(inp, dev)
+    names = [n for n in EXTRA_WORKLOADS if n != args.workload] if not args.no_extra else []
+    # inputs are drawn on the CPU before the GPU phase starts
+    inputs = {n: make_inputs(WORKLOADS[n]) for n in [args.workload] + names}
+    steps_of = {n: st for n, st in ((n, DecodeStep.create(inputs[n], dev)) for n in inputs)}
+    fl = Flusher(dev)
     k = spec.n_drafts
     stream = torch.cuda.current_stream()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_w = torch.empty(int(1.5 * l2), dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(int(1.5 * l2) // 4, dtype=torch.float32, device=dev)
-    flush_out = torch.empty((), dtype=torch.float32, device=dev)
-
-    def flush_read():
-        torch.sum(flush_r, dim=0, out=flush_out)
-
-    def flush(i):  # between steps: write (dirty lines), then read (clean them out)
-        flush_w.fill_(i & 0xFF)
-        flush_read()
-
-    def ev():
-        return torch.cuda.Event(enable_timing=True)
-
-    # ---------------- device-resident timing
-    for i in range(args.warmup):
-        flush(i)
-        st.run()
-    barrier()
     sampler = ClockSampler(local) if rank == 0 else None
-    marks = []
-    for i in range(args.steps):
-        flush(i)
-        e = [ev() for _ in range(3 + 2 * k)]
-        e[0].record(stream)
-        st.verify()
-        e[1].record(stream)
-        st.select()
-        e[2].record(stream)
-        for t in range(1, k + 1):
-            flush_read()
-            e[1 + 2 * t].record(stream)
-            st.draft(t)
-            e[2 + 2 * t].record(stream)
-        marks.append(e)
-    barrier()
-    clocks = sampler.stop() if sampler else None
-    assert int(st.error_flag.item()) == 0, "device error flag set"
-    ver = [m[0].elapsed_time(m[1]) * 1e3 for m in marks]
-    sel = [m[1].elapsed_time(m[2]) * 1e3 for m in marks]
-    dra = [sum(m[1 + 2 * t].elapsed_time(m[2 + 2 * t]) * 1e3 for t in range(1, k + 1))
-           for m in marks]
-    step_us = [a + b + c for a, b, c in zip(ver, sel, dra)]
-    local_val = statistics.mean(step_us)
+    st = steps_of[args.workload]
+
+    # ---------------- the headline workload: K cold steps
+    m = measure(spec, inputs[args.workload], st, fl, args.steps, args.warmup, barrier, dev)
 
     # ---------------- hot: the step back to back, no flushes, replayed as a
     # CUDA graph so that host launch cost is not in the number
-    barrier()
     graph = torch.cuda.CUDAGraph()
     cap_stream = torch.cuda.Stream(dev)
     cap_stream.wait_stream(stream)
     with torch.cuda.stream(cap_stream):
-        st.run(cap_stream)  # bind the capture stream's arguments outside capture
+        st.run(cap_stream)
         torch.cuda.synchronize()
         with torch.cuda.graph(graph, stream=cap_stream):
             st.run(cap_stream)
     stream.wait_stream(cap_stream)
     barrier()
-    n_hot = min(args.steps, 500)
-    for _ in range(3):
-        graph.replay()
-    h0, h1 = ev(), ev()
-    h0.record(stream)
-    for _ in range(n_hot):
-        graph.replay()
-    h1.record(stream)
-    barrier()
-    hot_us = h0.elapsed_time(h1) * 1e3 / n_hot
+    hot_us = time_graph(graph, min(args.steps, 200), barrier)
+    del graph
 
     # ---------------- end to end through the C ABI with host buffers: every
     # step copies its inputs (verify and draft queries, one pinned buffer) to
     # the device and reads its results (attention outputs; indices and
-    # counts) back, inside the timed region
+    # counts) back.  Device-timed: event pairs around [H2D, verify, select],
+    # each draft call and [D2H]; the L2 flushes between them are left out.
     in_h = torch.empty(st.io_in.shape, dtype=st.io_in.dtype).pin_memory()
     in_h.copy_(st.io_in.cpu())
     out_h = torch.empty(st.io_out.shape, dtype=st.io_out.dtype).pin_memory()
@@ -499,17 +647,17 @@ def main():
     h2d = in_h.numel() * in_h.element_size()
     d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
     e2e_marks = []
-    n_e2e = min(args.steps, 500)
+    n_e2e = min(args.steps, 200)
     for i in range(n_e2e + args.warmup):
-        flush(i)
-        e = [ev() for _ in range(4 + 2 * k)]
+        fl.full(i)
+        e = _events(4 + 2 * k)
         e[0].record(stream)
         st.io_in.copy_(in_h, non_blocking=True)
         st.verify()
         st.select()
         e[1].record(stream)
         for t in range(1, k + 1):
-            flush_read()
+            fl.read()
             e[2 * t].record(stream)
             st.draft(t)
             e[2 * t + 1].record(stream)
@@ -521,7 +669,7 @@ def main():
             e2e_marks.append(e)
     barrier()
     e2e_us = statistics.mean(
-        sum(m[2 * j].elapsed_time(m[2 * j + 1]) for j in range(k + 2)) * 1e3 for m in e2e_marks)
+        sum(m_[2 * j].elapsed_time(m_[2 * j + 1]) for j in range(k + 2)) * 1e3 for m_ in e2e_marks)
     ix_h = sel_h[:st.indices.numel()].view(st.indices.shape)
     assert torch.equal(ix_h, st.indices.cpu())
 
@@ -534,8 +682,8 @@ def main():
         out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
         ts = []
         for i in range(reps + 3):
-            flush(i)
-            a, b_ = ev(), ev()
+            fl.full(i)
+            a, b_ = _events(2)
             a.record(stream)
             vg.verify_attention(st.kv, q, st.prefix_lens, spec.max_prefix, spec.softmax_scale,
                                 out, mode, capture, 0, ws, st.error_flag)
@@ -588,8 +736,8 @@ def main():
         blocks.shape[-1]), dev)
     sv_t = []
     for i in range(33):
-        flush(i)
-        a, b_ = ev(), ev()
+        fl.full(i)
+        a, b_ = _events(2)
         a.record(stream)
         vg.sparse_verify_attention(st.kv, st.q_verify, st.prefix_lens, spec.max_prefix,
                                    spec.softmax_scale, bl_d, ct_d, out_sv, workspace=ws_sv,
@@ -617,42 +765,58 @@ def main():
     del ws_sv, out_sv
     assert int(st.error_flag.item()) == 0, "device error flag set"
 
-    value, e2e_val, hot_val = reduce_max([local_val, e2e_us, hot_us], world, dev)
+    # ---------------- the other workloads: the same cold-step timings
+    others = {}
+    for n in names:
+        s_o = WORKLOADS[n]
+        mo = measure(s_o, inputs[n], steps_of[n], fl, min(args.steps, 50), 3, barrier, dev)
+        others[n] = (s_o, mo)
+    clocks = sampler.stop() if sampler else None
+
+    flat = [m["value"], e2e_us, hot_us, m["stages_us"]["verify"]]
+    for n in names:
+        flat += [others[n][1]["value"], others[n][1]["stages_us"]["verify"]]
+    red = reduce_max(flat, world, dev)
+    m["value"], e2e_val, hot_val, m["stages_us"]["verify"] = red[:4]
+    for i, n in enumerate(names):
+        others[n][1]["value"], others[n][1]["stages_us"]["verify"] = red[4 + 2 * i:6 + 2 * i]
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    nb = algorithmic_bytes(spec)
     peak, peak_kind = measured_peaks()
-    v_mean = statistics.mean(ver)
-    achieved = nb["verify"] / (v_mean * 1e-6) / 1e9
+    head = summarize(spec, m, peak, peak_kind, st.launches_per_step())
     res = {
-        "metric": METRIC, "metric_desc": METRIC_DESC, "value": value, "unit": "us",
+        "metric": METRIC, "metric_desc": METRIC_DESC, "value": head["value"], "unit": "us",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
+        "ms_per_step": head["value"] / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; see workloads.py)",
         "config": _config(spec, world),
-        "hbm_gbs_step": nb["step"] / (value * 1e-6) / 1e9,
-        "hbm_frac_step": nb["step"] / (value * 1e-6) / 1e9 / peak,
-        "stages_us": {"verify": v_mean, "select": statistics.mean(sel),
-                      "drafts_total": statistics.mean(dra),
-                      "draft_each": statistics.mean(dra) / max(k, 1)},
-        "stages_bytes": nb,
+        "timing": "value: cold step as a replayed CUDA graph (flushes + step kernels) minus "
+                  "the same graph with flushes only, mean over the timed replays; stages_us: "
+                  "event pair around every eagerly launched call",
+    }
+    res.update({key: val for key, val in head.items() if key != "value"})
+    res.update({
         "hot_us_per_step": hot_val,
-        "roofline": {"kernel": "verify_kernel", "bound": "hbm", "achieved": achieved,
-                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
-                     "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": verify_traffic(spec.name)},
         "e2e": {"value": e2e_val, "unit": "us", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "timing": "device events around [H2D + verify + select], each draft call and "
+                          "[D2H], issued through the C ABI from Python; L2 flushes between "
+                          "them excluded; host-side completion not included"},
         "gpu_launches": args.steps * st.launches_per_step(),
         "capture_rules": capture_study,
         "sparse_verification": sparse_study,
-        "projection": speedup_projection(0.7, k, statistics.mean(dra) / max(k, 1), v_mean,
-                                         statistics.mean(sel), t_dense),
+        # per-call event times throughout (the dense decode step is timed
+        # the same way)
+        "projection": speedup_projection(0.7, k, head["stages_us"]["draft_each"],
+                                         head["stages_us"]["verify"],
+                                         head["stages_us"]["select"], t_dense),
+        "workloads": {n: summarize(others[n][0], others[n][1], peak, peak_kind,
+                                   steps_of[n].launches_per_step()) for n in names},
         "clocks": clocks,
-    }
+    })
     if not args.no_cpu_baseline:
         try:
             res["cpu_baseline"] = cpu_baseline(spec.name)

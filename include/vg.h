@@ -30,9 +30,12 @@
  *     the offending load or sequence; nothing traps.
  *   - Workspaces: sized by the matching *_workspace_bytes() call for the same
  *     arguments on the same device (0 = none needed, the pointer may be
- *     NULL).  They need no initialisation: everything in them is written
- *     before it is read.  Calls that share a workspace must not overlap in
- *     time.
+ *     NULL).  Calls that share a workspace must not overlap in time.  The
+ *     verify and select workspaces need no initialisation: everything in
+ *     them is written before it is read.  The sparse-draft workspace starts
+ *     with completion counters that must be zero before its first use
+ *     (cudaMemsetAsync once after allocating it); every call leaves them
+ *     zero again.
  */
 #ifndef VG_H_
 #define VG_H_
@@ -132,7 +135,7 @@ typedef struct vg_paged_kv {
  *                written, the rest of each row is left untouched.  May be
  *                NULL with VG_CAPTURE_NONE.
  *   num_splits   0 = automatic; otherwise the number of KV-length splits
- *                (clamped to the number of 64-position tiles).  Results agree
+ *                (clamped to the number of 128-position tiles).  Results agree
  *                across split counts up to float32 rounding.  With more than
  *                one split, the call launches a second, small merge kernel
  *                (programmatic dependent launch) on the same stream.
@@ -212,6 +215,14 @@ vg_status vg_sparse_verify_attention(const vg_paged_kv* kv, const void* q,
  *   indices  int32 [batch][rows][cap], ascending, entries past the count = -1.
  *   counts   int32 [batch][rows].
  *   cap      >= min(max_prefix, n_sink + n_recent + top_k).
+ *   kv, slots  optional (both NULL, or both given): slots int32
+ *            [batch][rows][cap] receives, beside each kept position p, its
+ *            cache slot page_table[b][p / 16] * 16 + p % 16 in kv's page
+ *            pool (-1 past the count, and -1 with VG_DEVERR_PAGE where the
+ *            page id is outside [0, num_pages)).  The translation is done
+ *            once per selection, so that vg_sparse_draft_attention reaches a
+ *            selected row in one dependent load.  kv->num_kv_heads must equal
+ *            num_kv_heads and kv->max_pages_per_seq * 16 >= max_prefix.
  *   workspace  vg_select_workspace_bytes() bytes: room for the positions'
  *            score keys (one 4-byte key per prefix position and selection
  *            row); no initialisation needed.
@@ -226,8 +237,8 @@ size_t vg_select_workspace_bytes(int batch, int num_kv_heads, int max_prefix, in
 vg_status vg_select_kv(const float* capture, int capture_mode, const int32_t* prefix_lens,
                        int batch, int num_q_heads, int num_kv_heads, int max_prefix, int top_k,
                        int n_sink, int n_recent, int per_head, int32_t* indices, int32_t* counts,
-                       int cap, void* workspace, size_t workspace_bytes, int32_t* error_flag,
-                       cudaStream_t stream);
+                       int cap, const vg_paged_kv* kv, int32_t* slots, void* workspace,
+                       size_t workspace_bytes, int32_t* error_flag, cudaStream_t stream);
 
 /* Weight-statistics variant of vg_select_kv (A Sparse Glimpse of the Whole,
  * "What carries the argument": rank positions by the attention weights of a
@@ -238,12 +249,13 @@ vg_status vg_select_kv(const float* capture, int capture_mode, const int32_t* pr
  *   (ascending) of expf(logits[q][i][j] - lse[q][i]),
  * i.e. the row-normalised post-softmax weights summed over the window (the
  * mean ranks identically); float32, fixed order.  Everything else --
- * candidates, sink/recent, ties, outputs, workspace, errors -- is as in
- * vg_select_kv. */
+ * candidates, sink/recent, ties, outputs, slots, workspace, errors -- is as
+ * in vg_select_kv. */
 vg_status vg_select_kv_weights(const float* capture, int n_rows, const int32_t* prefix_lens,
                                int batch, int num_q_heads, int num_kv_heads, int max_prefix,
                                int top_k, int n_sink, int n_recent, int per_head,
-                               int32_t* indices, int32_t* counts, int cap, void* workspace,
+                               int32_t* indices, int32_t* counts, int cap,
+                               const vg_paged_kv* kv, int32_t* slots, void* workspace,
                                size_t workspace_bytes, int32_t* error_flag, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
@@ -256,25 +268,37 @@ vg_status vg_select_kv_weights(const float* capture, int n_rows, const int32_t* 
  *               sequence, at position cur_len[b] - 1.
  *   indices, counts  as written by vg_select_kv (per_head must match);
  *               every index must be < tail_start[b].
+ *   slots       NULL, or the cache slots vg_select_kv wrote beside the
+ *               indices (same shape): the K/V row of a selected entry is
+ *               then read at its slot without a page-table lookup.  A slot
+ *               whose offset within its page differs from its index's is
+ *               flagged VG_DEVERR_INDEX and skipped.  Slots stay valid while
+ *               the page-table entries of the selected positions do not
+ *               change (new pages for the tail do not matter).
  *   tail_start  int32 [batch]: the prefix length the selection was made on.
  *   cur_len     int32 [batch]: query position + 1; tail = [tail_start,
- *               cur_len), 0 <= cur_len - tail_start <= max_tail.
+ *               cur_len), 0 <= cur_len - tail_start <= max_tail.  The tail's
+ *               rows are always reached through the page table.
  *   out         bf16 [batch][num_q_heads][head_dim]; zero when nothing is
  *               attended (count 0 and an empty tail).
- * The attended list (selection, then tail) is processed in chunks of 64
- * entries, one CTA each, which write fp32 partials to the workspace; a
- * second, small kernel (programmatic dependent launch, same stream) merges
- * them into `out`.
+ *   workspace   vg_sparse_draft_workspace_bytes(); zero-filled before its
+ *               first use (see the conventions above).  If a call flags
+ *               VG_DEVERR_TIMEOUT, zero it again before the next call.
+ * One kernel: the attended list (selection, then tail) is processed in
+ * chunks of 128 entries, one CTA each.  A list of one chunk writes `out`
+ * directly; otherwise every chunk writes an fp32 record (m, l, O) to the
+ * workspace and the chunk that completes a (sequence, KV head) merges them
+ * into `out`.
  * Supported: head_dim 64/128, g in [1, 8], cap + max_tail <= 65536.
  * ------------------------------------------------------------------------- */
 size_t vg_sparse_draft_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
                                        int head_dim, int cap, int max_tail);
 
 vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void* q, const int32_t* indices,
-                                    const int32_t* counts, int per_head, int cap,
-                                    const int32_t* tail_start, const int32_t* cur_len, int batch,
-                                    int num_q_heads, int max_tail, float softmax_scale, void* out,
-                                    void* workspace, size_t workspace_bytes,
+                                    const int32_t* slots, const int32_t* counts, int per_head,
+                                    int cap, const int32_t* tail_start, const int32_t* cur_len,
+                                    int batch, int num_q_heads, int max_tail, float softmax_scale,
+                                    void* out, void* workspace, size_t workspace_bytes,
                                     int32_t* error_flag, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
@@ -293,6 +317,9 @@ vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void* q, const 
  * VG_ERR_WORKSPACE_TOO_SMALL before anything is launched; use
  * vg_verify_attention with a caller workspace for those.
  *
+ *   - The scratch array belongs to the CURRENT device: call with the
+ *     device of `stream` current (a stream of another device is rejected
+ *     with VG_ERR_INVALID_ARGUMENT before anything is launched).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.

@@ -45,6 +45,9 @@ struct SelectParams {
   const int32_t* prefix_lens;
   int32_t* indices;
   int32_t* counts;
+  int32_t* slots;              // NULL, or cache slots beside the indices
+  const int32_t* page_table;   // with slots: [batch][max_pages_per_seq]
+  int max_pages_per_seq, num_pages;
   int32_t* error_flag;
   int capture_mode, batch, num_q_heads, num_kv_heads, group, max_prefix;
   int top_k, n_sink, n_recent, per_head, cap, rows, slice;
@@ -57,6 +60,23 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Writes kept position `pos` to list slot `k` and, when slots are asked for,
+// its cache slot (physical page * 16 + offset) from the CTA's staged
+// page-table entries pt_s (logical pages pt0, pt0 + 1, ...).
+__device__ __forceinline__ void put_kept(const SelectParams& p, int32_t* out, int32_t* sout,
+                                         const int32_t* pt_s, int pt0, int k, int pos) {
+  out[k] = pos;
+  if (sout) {
+    const int phys = pt_s[pos / 16 - pt0];
+    int v = -1;
+    if (phys >= 0 && phys < p.num_pages)
+      v = phys * 16 + (pos & 15);
+    else
+      flag_error(p.error_flag, VG_DEVERR_PAGE);
+    sout[k] = v;
+  }
 }
 
 // Score of prefix position j for selection row `row` of sequence b, summed in
@@ -167,24 +187,38 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   uint32_t* recv = reinterpret_cast<uint32_t*>(sel_smem + ((p.slice * 4 + 15) & ~15));
   uint4* crecv = reinterpret_cast<uint4*>(recv + 4 * kMaxCluster * 256);
   uint64_t* mb = reinterpret_cast<uint64_t*>(crecv + kMaxCluster);
+  int32_t* pt_s = reinterpret_cast<int32_t*>(mb + 6);  // page-table entries of the slice
 
   // programmatic dependent launch: the capture comes from the previous kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
+  const int lo = rank * p.slice;
+  // the slice's page-table entries, for the cache slots of kept positions
+  // (loaded while the length is in flight; pages past the row are not read)
+  const int pt0 = lo / 16;
+  if (p.slots) {
+    const int npt = min((lo + p.slice - 1) / 16, p.max_pages_per_seq - 1) - pt0 + 1;
+    const int32_t* ptr = p.page_table + (size_t)b * p.max_pages_per_seq + pt0;
+    for (int i = tid; i < npt; i += blockDim.x) pt_s[i] = __ldg(ptr + i);
+  }
   const int L = p.prefix_lens[b];
   int32_t* out = p.indices + ((size_t)b * p.rows + row) * p.cap;
+  int32_t* sout = p.slots ? p.slots + ((size_t)b * p.rows + row) * p.cap : nullptr;
   if (L < 0 || L > p.max_prefix) {  // same decision in every CTA of the cluster
     if (tid == 0 && rank == 0) flag_error(p.error_flag, VG_DEVERR_LENGTH);
     return;
   }
   const int budget = p.n_sink + p.n_recent + p.top_k;
-  const int lo = rank * p.slice;
   const int n_loc = max(0, min(lo + p.slice, L) - lo);
 
   if (L <= budget) {  // every prefix position is kept
-    for (int j = tid; j < n_loc; j += blockDim.x) out[lo + j] = lo + j;
+    __syncthreads();  // the staged page-table entries are visible
+    for (int j = tid; j < n_loc; j += blockDim.x) put_kept(p, out, sout, pt_s, pt0, lo + j, lo + j);
     if (rank == 0) {
-      for (int j = L + tid; j < p.cap; j += blockDim.x) out[j] = -1;
+      for (int j = L + tid; j < p.cap; j += blockDim.x) {
+        out[j] = -1;
+        if (sout) sout[j] = -1;
+      }
       if (tid == 0) p.counts[(size_t)b * p.rows + row] = L;
     }
     return;
@@ -408,23 +442,32 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
       const unsigned eb = __ballot_sync(0xffffffffu, is_eq);
       const bool sel = (in && k > T) || (is_eq && eq_run + __popc(eb & lt_mask) < krem);
       const unsigned sbal = __ballot_sync(0xffffffffu, sel);
-      if (sel) out[slot0 + sel_run + __popc(sbal & lt_mask)] = pos;
+      if (sel) put_kept(p, out, sout, pt_s, pt0, slot0 + sel_run + __popc(sbal & lt_mask), pos);
       sel_run += __popc(sbal);
       eq_run += __popc(eb);
     }
   }
+  // sink and recent positions, by the CTA whose slice holds them
+  for (int j = tid; j < n_loc; j += blockDim.x) {
+    const int pos = lo + j;
+    if (pos < p.n_sink)
+      put_kept(p, out, sout, pt_s, pt0, pos, pos);
+    else if (pos >= L - p.n_recent)
+      put_kept(p, out, sout, pt_s, pt0, p.n_sink + p.top_k + (pos - (L - p.n_recent)), pos);
+  }
   if (rank == 0) {
-    for (int j = tid; j < p.n_sink; j += blockDim.x) out[j] = j;
-    for (int j = tid; j < p.n_recent; j += blockDim.x)
-      out[p.n_sink + p.top_k + j] = L - p.n_recent + j;
-    for (int j = budget + tid; j < p.cap; j += blockDim.x) out[j] = -1;
+    for (int j = budget + tid; j < p.cap; j += blockDim.x) {
+      out[j] = -1;
+      if (sout) sout[j] = -1;
+    }
     if (tid == 0) p.counts[(size_t)b * p.rows + row] = budget;
   }
   cluster_wait_acquire();
 }
 
 size_t select_smem_bytes(int slice) {
-  return align_up((size_t)slice * 4, 16) + 4 * kMaxCluster * 256 * 4 + kMaxCluster * 16 + 5 * 8;
+  return align_up((size_t)slice * 4, 16) + 4 * kMaxCluster * 256 * 4 + kMaxCluster * 16 + 6 * 8 +
+         align_up(((size_t)slice / 16 + 2) * 4, 16);
 }
 
 bool select_shape(int max_prefix, int* C, int* slice) {
@@ -453,45 +496,53 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
                              const int32_t* prefix_lens, int batch, int num_q_heads,
                              int num_kv_heads, int max_prefix, int top_k, int n_sink,
                              int n_recent, int per_head, int32_t* indices, int32_t* counts,
-                             int cap, void* workspace, size_t workspace_bytes,
-                             int32_t* error_flag, cudaStream_t stream);
+                             int cap, const vg_paged_kv* kv, int32_t* slots, void* workspace,
+                             size_t workspace_bytes, int32_t* error_flag, cudaStream_t stream);
 
 extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
                                   const int32_t* prefix_lens, int batch, int num_q_heads,
                                   int num_kv_heads, int max_prefix, int top_k, int n_sink,
                                   int n_recent, int per_head, int32_t* indices, int32_t* counts,
-                                  int cap, void* workspace, size_t workspace_bytes,
-                                  int32_t* error_flag, cudaStream_t stream) {
+                                  int cap, const vg_paged_kv* kv, int32_t* slots,
+                                  void* workspace, size_t workspace_bytes, int32_t* error_flag,
+                                  cudaStream_t stream) {
   if (capture_mode == VG_CAPTURE_ALL_SUM) capture_mode = VG_CAPTURE_GROUP_SUM;  // same layout
   if (capture_mode != VG_CAPTURE_GROUP_SUM && capture_mode != VG_CAPTURE_ROWS)
     return VG_ERR_INVALID_ARGUMENT;
   return select_impl(capture, capture_mode, 0, prefix_lens, batch, num_q_heads, num_kv_heads,
-                     max_prefix, top_k, n_sink, n_recent, per_head, indices, counts, cap,
-                     workspace, workspace_bytes, error_flag, stream);
+                     max_prefix, top_k, n_sink, n_recent, per_head, indices, counts, cap, kv,
+                     slots, workspace, workspace_bytes, error_flag, stream);
 }
 
 extern "C" vg_status vg_select_kv_weights(const float* capture, int n_rows,
                                           const int32_t* prefix_lens, int batch, int num_q_heads,
                                           int num_kv_heads, int max_prefix, int top_k, int n_sink,
                                           int n_recent, int per_head, int32_t* indices,
-                                          int32_t* counts, int cap, void* workspace,
+                                          int32_t* counts, int cap, const vg_paged_kv* kv,
+                                          int32_t* slots, void* workspace,
                                           size_t workspace_bytes, int32_t* error_flag,
                                           cudaStream_t stream) {
   if (n_rows <= 0 || n_rows > 16) return VG_ERR_INVALID_ARGUMENT;
   return select_impl(capture, VG_CAPTURE_ALL_ROWS, n_rows, prefix_lens, batch, num_q_heads,
                      num_kv_heads, max_prefix, top_k, n_sink, n_recent, per_head, indices, counts,
-                     cap, workspace, workspace_bytes, error_flag, stream);
+                     cap, kv, slots, workspace, workspace_bytes, error_flag, stream);
 }
 
 static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
                              const int32_t* prefix_lens, int batch, int num_q_heads,
                              int num_kv_heads, int max_prefix, int top_k, int n_sink,
                              int n_recent, int per_head, int32_t* indices, int32_t* counts,
-                             int cap, void* workspace, size_t workspace_bytes,
-                             int32_t* error_flag, cudaStream_t stream) {
+                             int cap, const vg_paged_kv* kv, int32_t* slots, void* workspace,
+                             size_t workspace_bytes, int32_t* error_flag, cudaStream_t stream) {
   if (!capture || !prefix_lens || !indices || !counts || batch <= 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || max_prefix <= 0 || top_k < 0 || n_sink < 0 || n_recent < 0 || cap <= 0)
     return VG_ERR_INVALID_ARGUMENT;
+  if (slots) {  // cache slots need the page table of the cache the positions index
+    const vg_status st = check_paged_kv(kv);
+    if (st != VG_OK) return st;
+    if (kv->num_kv_heads != num_kv_heads || ceil_div(max_prefix, kPageSize) > kv->max_pages_per_seq)
+      return VG_ERR_INVALID_ARGUMENT;
+  }
   if (num_q_heads % num_kv_heads) return VG_ERR_INVALID_ARGUMENT;
   if (num_q_heads / num_kv_heads > 8) return VG_ERR_UNSUPPORTED;
   const long long budget = (long long)n_sink + n_recent + top_k;
@@ -507,6 +558,10 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
   p.prefix_lens = prefix_lens;
   p.indices = indices;
   p.counts = counts;
+  p.slots = slots;
+  p.page_table = slots ? kv->page_table : nullptr;
+  p.max_pages_per_seq = slots ? kv->max_pages_per_seq : 0;
+  p.num_pages = slots ? kv->num_pages : 0;
   p.error_flag = error_flag;
   p.capture_mode = capture_mode;
   p.n_rows = n_rows;

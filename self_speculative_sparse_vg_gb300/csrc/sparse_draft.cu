@@ -7,33 +7,39 @@
 // Whole, "What carries the argument": the dense cache is kept, the index is a
 // view into it.
 //
-// Design: one CTA per 64-entry chunk of the attended list (the selection,
-// then the tail [tail_start, cur_len)), per (KV head, sequence); all chunks of
-// a step are resident at once.
-//  * The chunk's selected positions, the sequence's page-table row (one bulk
-//    copy into shared memory when short), the query rows and the lengths are
-//    loaded together, so a row's address costs one round trip.
-//  * The chunk's K and V rows (256 bytes each at head_dim 128) are then
-//    gathered with 16-byte cp.async pieces, consecutive threads on
-//    consecutive pieces of a row, into a row-padded tile (row stride
-//    head_dim * 2 + 16 bytes, so ldmatrix rows fall in distinct bank groups).
-//  * The g query heads of the KV head are the rows of a 16-row bf16
-//    mma.sync tile (zero padded); warp w takes positions [16w, 16w + 16),
-//    and P is reused as the A operand of P.V.
-//  * Each CTA writes an fp32 partial (m, l, O) to the workspace; a small
-//    merge kernel, chained with programmatic dependent launch, combines the
-//    chunks of each (sequence, KV head, query head).
+// Design: one kernel per draft step.  One CTA per CH-entry chunk of the
+// attended list (the selection, then the tail [tail_start, cur_len)), per
+// (KV head, sequence); all chunks of a step are resident at once.
+//  * Addresses cost one round trip.  With the cache slots the selector wrote
+//    beside the positions (physical page * 16 + offset, translated once per
+//    selection), a chunk loads its slots, its positions (checked against the
+//    prefix), the query rows and the lengths together.  Without slots the
+//    sequence's page-table row is staged in shared memory in the same round
+//    trip (one bulk copy when it is short).  Only the few tail entries look
+//    their page up after the lengths are known.
+//  * The chunk's K and V rows (256 bytes each at head_dim 128) are gathered
+//    with 16-byte cp.async pieces, consecutive threads on consecutive pieces
+//    of a row, into row-padded tiles (row stride head_dim * 2 + 16 bytes, so
+//    ldmatrix rows fall in distinct bank groups).
+//  * The g query heads of the KV head are the rows of a 16-row bf16 mma.sync
+//    tile (zero padded); warp w takes positions [16w, 16w + 16), and P is
+//    reused as the A operand of P.V.
+//  * A list of one chunk writes the output directly.  Otherwise each CTA
+//    writes an fp32 record (m, l, unnormalised O per query head) to the
+//    workspace and takes a ticket from a per-(sequence, KV head) counter; the
+//    CTA that draws the last ticket merges every record by log-sum-exp,
+//    writes the output and puts the counter back to zero.  No CTA waits for
+//    another and no second kernel is launched.
 #include "vg_device.cuh"
 #include "vg_host.h"
 
 namespace vg {
 namespace {
 
-constexpr int kChunk = 64;  // attended entries per CTA
-constexpr int kDraftWarps = 4;
-constexpr int kDraftThreads = kDraftWarps * 32;
-constexpr int kPtMax = 2048;  // page-table entries staged in shared memory (8 KB)
-constexpr int kMaxChunks = 1024;
+constexpr int kChunk = 128;          // attended entries per CTA
+constexpr int kMaxEntries = 65536;   // cap + max_tail
+constexpr int kPtMax = 2048;         // page-table entries staged in shared memory (no slots)
+constexpr int kRecHead = 16;         // floats before O in a chunk record: m[8], l[8]
 
 struct DraftParams {
   const __nv_bfloat16* k_pages;
@@ -41,30 +47,36 @@ struct DraftParams {
   const int32_t* page_table;
   const __nv_bfloat16* q;
   const int32_t* indices;
+  const int32_t* slots;    // NULL: translate positions through the page table
   const int32_t* counts;
   const int32_t* tail_start;
   const int32_t* cur_len;
   __nv_bfloat16* out;
-  float* part_o;   // [B][Hkv][chunks][g][HD]
-  float* part_ml;  // [B][Hkv][chunks][g][2]
+  float* records;          // [B][Hkv][chunks][rec_floats]
+  int32_t* tickets;        // [B][Hkv], zero between calls
   int32_t* error_flag;
   int batch, num_q_heads, num_kv_heads, group, per_head, cap, max_tail;
-  int num_pages, max_pages_per_seq, chunks, pt_cap;
+  int num_pages, max_pages_per_seq, chunks, rec_floats;
   float scale_log2;
 };
 
-template <int HD>
+template <int HD, int CH>
 struct DraftLayout {
+  static constexpr int kWarps = CH / 16;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int kRowBytes = HD * 2 + 16;             // padded K / V / Q row
-  static constexpr int kTileBytes = kChunk * kRowBytes;     // one of K / V
+  static constexpr int kTileBytes = CH * kRowBytes;         // one of K / V
   static constexpr int kQBytes = 16 * kRowBytes;
   static constexpr int kOStride = 2 * 32 + 8;               // floats per (warp, n-tile) stash
-  static constexpr size_t kBytes = 1024 + 2 * (size_t)kTileBytes + kQBytes + (size_t)kPtMax * 4 + 64;
-  static_assert((size_t)kDraftWarps * (HD / 8) * kOStride * 4 <= 2 * (size_t)kTileBytes,
+  static constexpr int kMergeBytes = 2 * kTileBytes;        // K/V tiles, reused by the merge
+  static constexpr size_t bytes(bool slots) {
+    return 128 + (size_t)kMergeBytes + kQBytes + (slots ? 0 : (size_t)kPtMax * 4) + 64;
+  }
+  static_assert((size_t)kWarps * (HD / 8) * kOStride * 4 <= (size_t)kMergeBytes,
                 "the O stash reuses the K/V tiles");
 };
 
-// Sequence-level checks shared by both kernels; false if the sequence is skipped.
+// Sequence-level checks; false if the sequence is skipped.
 __device__ __forceinline__ bool draft_lengths(const DraftParams& p, int b, int row, int rows,
                                               int* cnt, int* ts, int* cl) {
   *cnt = p.counts[(size_t)b * rows + row];
@@ -77,69 +89,189 @@ __device__ __forceinline__ bool draft_lengths(const DraftParams& p, int b, int r
   return true;
 }
 
-template <int HD>
-__global__ void __launch_bounds__(kDraftThreads)
+// Log-sum-exp merge of the nch chunk records of one (sequence, KV head) by
+// the CTA that drew the last ticket.  Records are staged through shared
+// memory a batch at a time (every load of a batch in flight together); warp
+// w forms the batch weights of query heads w, w + NW, ...; thread t then
+// accumulates float4 column (t mod HD/4) of head t / (HD/4), and more items
+// when there are fewer threads than g * HD / 4.
+template <int HD, int NT>
+__device__ __forceinline__ void merge_records(const DraftParams& p, const float* src, int nch,
+                                              __nv_bfloat16* dst, uint8_t* area, int area_bytes,
+                                              float* mrun_s, float* lrun_s, float* corr_s) {
+  constexpr int C4 = HD / 4;
+  constexpr int NW = NT / 32;
+  constexpr int IPT = (8 * C4 + NT - 1) / NT;  // items per thread at g = 8
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = p.group, RF = p.rec_floats;
+  const int cpb = (area_bytes - 64) / (RF * 4 + 32);  // chunks per batch (w_s: 8 floats each)
+  float* recs = reinterpret_cast<float*>(area);
+  float* w_s = recs + (size_t)cpb * RF;
+  if (tid < 8) {
+    mrun_s[tid] = -INFINITY;
+    lrun_s[tid] = 0.f;
+  }
+  float4 acc[IPT];
+#pragma unroll
+  for (int i = 0; i < IPT; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < nch; c0 += cpb) {
+    const int nb = min(cpb, nch - c0);
+    const int n4 = nb * RF / 4;
+    const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)c0 * RF);
+    float4* d4 = reinterpret_cast<float4*>(recs);
+    for (int base = 0; base < n4; base += NT * 8) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = base + k * NT + tid;
+        v[k] = i < n4 ? __ldcg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = base + k * NT + tid;
+        if (i < n4) d4[i] = v[k];
+      }
+    }
+    __syncthreads();
+    for (int qi = warp; qi < g; qi += NW) {
+      float mb = -INFINITY;
+      for (int c = lane; c < nb; c += 32) mb = fmaxf(mb, recs[(size_t)c * RF + qi]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+      const float m_old = mrun_s[qi];
+      const float m_new = fmaxf(m_old, mb);
+      const float ref = safe_ref(m_new);
+      float lb = 0.f;
+      for (int c = lane; c < nb; c += 32) {
+        const float w = ex2(recs[(size_t)c * RF + qi] - ref);  // 0 for an empty chunk
+        w_s[c * 8 + qi] = w;
+        lb += w * recs[(size_t)c * RF + 8 + qi];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
+      if (lane == 0) {
+        const float corr = ex2(m_old - ref);  // 0 while nothing was accumulated
+        corr_s[qi] = corr;
+        mrun_s[qi] = m_new;
+        lrun_s[qi] = lrun_s[qi] * corr + lb;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < IPT; ++it) {
+      const int i = tid + it * NT;
+      if (i < g * C4) {
+        const int qi = i / C4, col = i - (i / C4) * C4;
+        const float corr = corr_s[qi];
+        float4 a = acc[it];
+        a.x *= corr;
+        a.y *= corr;
+        a.z *= corr;
+        a.w *= corr;
+        for (int c = 0; c < nb; ++c) {
+          const float w = w_s[c * 8 + qi];
+          const float4 o =
+              *reinterpret_cast<const float4*>(recs + (size_t)c * RF + kRecHead + qi * HD + col * 4);
+          a.x += w * o.x;
+          a.y += w * o.y;
+          a.z += w * o.z;
+          a.w += w * o.w;
+        }
+        acc[it] = a;
+      }
+    }
+    __syncthreads();  // the staging area is rewritten by the next batch
+  }
+#pragma unroll
+  for (int it = 0; it < IPT; ++it) {
+    const int i = tid + it * NT;
+    if (i < g * C4) {
+      const int qi = i / C4, col = i - (i / C4) * C4;
+      const float lt = lrun_s[qi];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float4 a = acc[it];
+      uint2 w;
+      w.x = pack_bf16(a.x * inv, a.y * inv);
+      w.y = pack_bf16(a.z * inv, a.w * inv);
+      *reinterpret_cast<uint2*>(dst + (size_t)qi * HD + col * 4) = w;
+    }
+  }
+}
+
+template <int HD, int CH, bool SLOTS>
+__global__ void __launch_bounds__(DraftLayout<HD, CH>::kThreads, 2)
     sparse_draft_kernel(const DraftParams p) {
-  using Lay = DraftLayout<HD>;
+  using Lay = DraftLayout<HD, CH>;
+  constexpr int NT = Lay::kThreads, NW = Lay::kWarps;
   constexpr int KS = HD / 16;  // k-steps of Q K^T
   constexpr int DN = HD / 8;   // O n-tiles
-  constexpr int CH = HD / 8;   // 16-byte chunks per row
+  constexpr int PC = HD / 8;   // 16-byte pieces per row
+  constexpr int RB = Lay::kRowBytes;
 
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = p.group;
   const int row = p.per_head ? h : 0;
   const int rows = p.per_head ? p.num_kv_heads : 1;
-  // programmatic dependent launch: indices and counts come from the previous
-  // kernel; the merge kernel may launch as soon as this grid has started
+  // programmatic dependent launch: indices, slots and counts come from the
+  // previous kernel; the next kernel may launch as soon as this grid runs
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  constexpr int RB = Lay::kRowBytes;
-  uint8_t* kt = smem;  // [64][RB]
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~uintptr_t(127));
+  uint8_t* kt = smem;  // [CH][RB]
   uint8_t* vt = kt + Lay::kTileBytes;
   uint8_t* qs = vt + Lay::kTileBytes;  // [16][RB]
-  int32_t* pt_s = reinterpret_cast<int32_t*>(qs + Lay::kQBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(pt_s + kPtMax);  // [0] page table
-  __shared__ long long off_s[kChunk];
-  __shared__ float wm_s[kDraftWarps][16], wl_s[kDraftWarps][16];
+  int32_t* pt_s = reinterpret_cast<int32_t*>(qs + Lay::kQBytes);  // no slots: page-table row
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pt_s + (SLOTS ? 0 : kPtMax));
+  __shared__ long long off_s[CH];
+  __shared__ float wm_s[NW][16], wl_s[NW][16];
+  __shared__ float mrun_s[8], lrun_s[8], corr_s[8];
+  __shared__ int last_s;
 
-  if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    fence_barrier_init();
+  if (!SLOTS) {
+    if (tid == 0) {
+      mbar_init(&bars[0], 1);
+      fence_barrier_init();
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // One round trip for everything the addresses depend on: this chunk's
-  // selected positions (read speculatively; the index array holds cap
-  // entries), the page-table row (one bulk copy when it is short), the
-  // query rows and the lengths.
-  const int e = chunk * kChunk + tid;
-  int pos_sel = -1;
-  if (tid < kChunk && e < p.cap) pos_sel = __ldg(p.indices + ((size_t)b * rows + row) * p.cap + e);
-  const bool pt_in_smem = p.max_pages_per_seq <= p.pt_cap;
-  if (pt_in_smem) {
-    const int32_t* src = p.page_table + (size_t)b * p.max_pages_per_seq;
-    const int n = p.max_pages_per_seq;
-    const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
-    const int nb = aligned ? (n / 4) * 4 : 0;  // entries in the bulk copy (whole 16 bytes)
-    if (tid == 0) {
-      if (nb > 0) {
-        mbar_arrive_expect_tx(&bars[0], nb * 4);
-        bulk_load(pt_s, src, nb * 4, &bars[0]);
-      } else {
-        mbar_arrive(&bars[0]);
-      }
-    }
-    for (int k = nb + tid; k < n; k += kDraftThreads) pt_s[k] = __ldg(src + k);
-  } else if (tid == 0) {
-    mbar_arrive(&bars[0]);
+  // selected positions and slots (read speculatively; the arrays hold cap
+  // entries), the query rows and the lengths (and, without slots, the
+  // page-table row).
+  const int e = chunk * CH + tid;
+  const size_t lrow = ((size_t)b * rows + row) * p.cap;
+  int pos_sel = -1, slot_sel = -1;
+  if (tid < CH && e < p.cap) {
+    pos_sel = __ldg(p.indices + lrow + e);
+    if (SLOTS) slot_sel = __ldg(p.slots + lrow + e);
   }
-  for (int idx = tid; idx < 16 * CH; idx += kDraftThreads) {  // query rows; rows >= g zero
-    const int r = idx / CH, ch = idx - (idx / CH) * CH;
+  const bool pt_in_smem = !SLOTS && p.max_pages_per_seq <= kPtMax;
+  if (!SLOTS) {
+    if (pt_in_smem) {
+      const int32_t* src = p.page_table + (size_t)b * p.max_pages_per_seq;
+      const int n = p.max_pages_per_seq;
+      const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+      const int nb = aligned ? (n / 4) * 4 : 0;  // entries in the bulk copy (whole 16 bytes)
+      if (tid == 0) {
+        if (nb > 0) {
+          mbar_arrive_expect_tx(&bars[0], nb * 4);
+          bulk_load(pt_s, src, nb * 4, &bars[0]);
+        } else {
+          mbar_arrive(&bars[0]);
+        }
+      }
+      for (int k = nb + tid; k < n; k += NT) pt_s[k] = __ldg(src + k);
+    } else if (tid == 0) {
+      mbar_arrive(&bars[0]);
+    }
+  }
+  for (int idx = tid; idx < 16 * PC; idx += NT) {  // query rows; rows >= g zero
+    const int r = idx / PC, ch = idx - (idx / PC) * PC;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < g)
       v = *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.num_q_heads + h * g + r) * HD + ch * 8);
@@ -147,62 +279,87 @@ __global__ void __launch_bounds__(kDraftThreads)
   }
   int cnt, ts, cl;
   const bool lengths_ok = draft_lengths(p, b, row, rows, &cnt, &ts, &cl);
-  // the page-table copy must land before anything reads it or the CTA leaves
-  if (!mbar_wait(&bars[0], 0)) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+  if (!SLOTS) {
+    // the page-table copy must land before anything reads it or the CTA
+    // leaves; a wait that gives up is reported and waited out once more
+    if (!mbar_wait(&bars[0], 0)) {
+      flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+      mbar_wait(&bars[0], 0);
+    }
+  }
+  __nv_bfloat16* out_bh = p.out + ((size_t)b * p.num_q_heads + h * g) * HD;
   if (!lengths_ok) {
     if (tid == 0 && chunk == 0)
       flag_error(p.error_flag, cnt < 0 || cnt > p.cap ? VG_DEVERR_COUNT : VG_DEVERR_LENGTH);
     return;
   }
   const int n_att = cnt + (cl - ts);
-  const int ne = min(kChunk, n_att - chunk * kChunk);
-  if (ne <= 0) return;  // past the end of this list: no partial
-  __syncthreads();
+  const int nch = (n_att + CH - 1) / CH;
+  if (n_att == 0) {  // nothing attended: the output is zero
+    if (chunk == 0)
+      for (int i = tid; i < g * HD / 2; i += NT)
+        reinterpret_cast<uint32_t*>(out_bh)[i] = 0u;
+    return;
+  }
+  const int ne = min(CH, n_att - chunk * CH);
+  if (ne <= 0) return;  // past the end of this list: no record, no ticket
+  __syncthreads();      // the page-table entries other threads copied are visible
 
-  // resolve each entry's K/V row and issue its two bulk copies; rows without
-  // an entry (past the list, bad index or page) are zero and masked below
-  if (tid < kChunk) {
+  // resolve each entry's K/V row; rows without an entry (past the list, bad
+  // index, slot or page) are zero and masked below
+  if (tid < CH) {
     long long off = -1;
     if (tid < ne) {
-      int pos = -1;
+      int phys = -1, sl = 0;
       if (e < cnt) {
-        pos = pos_sel;
-        if (pos < 0 || pos >= ts) {
+        const int pos = pos_sel;
+        // a slot must address the position's own offset within its page
+        const bool ok = pos >= 0 && pos < ts &&
+                        !(SLOTS && slot_sel >= 0 && (slot_sel & 15) != (pos & 15));
+        if (!ok) {
           flag_error(p.error_flag, VG_DEVERR_INDEX);
-          pos = -1;
+        } else {
+          if (SLOTS) {
+            phys = slot_sel < 0 ? -1 : slot_sel >> 4;
+            sl = slot_sel & 15;
+          } else {
+            phys = pt_in_smem
+                       ? pt_s[pos / kPageSize]
+                       : __ldg(p.page_table + (size_t)b * p.max_pages_per_seq + pos / kPageSize);
+            sl = pos % kPageSize;
+          }
+          if (phys < 0 || phys >= p.num_pages) flag_error(p.error_flag, VG_DEVERR_PAGE);
         }
       } else {
-        pos = ts + (e - cnt);
+        const int pos = ts + (e - cnt);  // tail: its page is looked up now
+        phys = pt_in_smem ? pt_s[pos / kPageSize]
+                          : __ldg(p.page_table + (size_t)b * p.max_pages_per_seq + pos / kPageSize);
+        sl = pos % kPageSize;
+        if (phys < 0 || phys >= p.num_pages) flag_error(p.error_flag, VG_DEVERR_PAGE);
       }
-      if (pos >= 0) {
-        const int phys =
-            pt_in_smem ? pt_s[pos / kPageSize]
-                       : __ldg(p.page_table + (size_t)b * p.max_pages_per_seq + pos / kPageSize);
-        if (phys >= 0 && phys < p.num_pages)
-          off = (((long long)phys * p.num_kv_heads + h) * kPageSize + (pos % kPageSize)) * HD;
-        else
-          flag_error(p.error_flag, VG_DEVERR_PAGE);
-      }
+      if (phys >= 0 && phys < p.num_pages)
+        off = (((long long)phys * p.num_kv_heads + h) * kPageSize + sl) * HD;
     }
     off_s[tid] = off;
     if (off < 0) {
       uint8_t* kd = kt + tid * RB;
       uint8_t* vd = vt + tid * RB;
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
+      for (int c = 0; c < PC; ++c) {
         *reinterpret_cast<uint4*>(kd + c * 16) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(vd + c * 16) = make_uint4(0, 0, 0, 0);
       }
     }
   }
-  __syncthreads();  // every row's offset is known
+  __syncthreads();  // every row's offset is known, the query rows are staged
   // gather: 16-byte cp.async pieces, consecutive threads on consecutive
   // pieces of a row (K rows, then V rows), all in flight at once
+  const int nrow = ((ne + 15) / 16) * 16;  // rows the warps read (zero past ne)
 #pragma unroll 4
-  for (int idx = tid; idx < 2 * kChunk * CH; idx += kDraftThreads) {
-    const int t = idx / (kChunk * CH);
-    const int rem = idx - t * (kChunk * CH);
-    const int rr = rem / CH, ch = rem - rr * CH;
+  for (int idx = tid; idx < 2 * nrow * PC; idx += NT) {
+    const int t = idx / (nrow * PC);
+    const int rem = idx - t * (nrow * PC);
+    const int rr = rem / PC, ch = rem - rr * PC;
     const long long off = off_s[rr];
     if (off >= 0)
       cp_async_16((t ? vt : kt) + rr * RB + ch * 16, (t ? p.v_pages : p.k_pages) + off + ch * 8);
@@ -299,56 +456,62 @@ __global__ void __launch_bounds__(kDraftThreads)
     }
   }
   __syncthreads();
-  // chunk partial: m, l and the unnormalised O relative to m, per query head
-  const size_t slot = (((size_t)b * p.num_kv_heads + h) * p.chunks + chunk) * g;
+  // chunk result per query head: m, l and the unnormalised O relative to m
+  float* rec = p.records + (((size_t)b * p.num_kv_heads + h) * p.chunks + chunk) * p.rec_floats;
   if (tid < g) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kDraftWarps; ++w) mx = fmaxf(mx, wm_s[w][tid]);
+    for (int w = 0; w < NW; ++w) mx = fmaxf(mx, wm_s[w][tid]);
     const float ref = safe_ref(mx);
     float lt = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDraftWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float wt = ex2(wm_s[w][tid] - ref);
       wm_s[w][tid] = wt;  // the warp's weight from here on
       lt += wt * wl_s[w][tid];
     }
-    p.part_ml[(slot + tid) * 2] = mx;
-    p.part_ml[(slot + tid) * 2 + 1] = lt;
+    wl_s[0][tid] = lt;   // read below, after the barrier (warp 0's l is no longer needed)
+    if (nch > 1) {
+      rec[tid] = mx;
+      rec[8 + tid] = lt;
+    }
   }
   __syncthreads();
-  for (int i = tid; i < g * HD; i += kDraftThreads) {
+  for (int i = tid; i < g * HD; i += NT) {
     const int qi = i / HD, d = i - (i / HD) * HD;
     float o = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDraftWarps; ++w)
+    for (int w = 0; w < NW; ++w)
       o += wm_s[w][qi] * sO[(w * DN + (d >> 3)) * OS + (qi * 4 + ((d & 7) >> 1)) * 2 + (d & 1)];
-    p.part_o[slot * HD + i] = o;
+    if (nch == 1) {  // the whole list: normalise and write the output
+      const float lt = wl_s[0][qi];
+      out_bh[i] = __float2bfloat16_rn(lt > 0.f ? o / lt : 0.f);
+    } else {
+      rec[kRecHead + i] = o;
+    }
   }
-}
+  if (nch == 1) return;
 
-// Chunk merge: one CTA per (query head, KV head, sequence); chained with
-// programmatic dependent launch.
-template <int HD>
-__global__ void __launch_bounds__(kMergeThreads) sparse_draft_merge_kernel(const DraftParams p) {
-  __shared__ __align__(16) float smem_f[kMergeSmemFloats];
-  const int qi = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int g = p.group;
-  const int row = p.per_head ? h : 0;
-  const int rows = p.per_head ? p.num_kv_heads : 1;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
-  int cnt, ts, cl;
-  if (!draft_lengths(p, b, row, rows, &cnt, &ts, &cl)) return;
-  const int nch = (cnt + (cl - ts) + kChunk - 1) / kChunk;
-  const size_t base = ((size_t)b * p.num_kv_heads + h) * p.chunks;
-  merge_splits<HD>(p.part_o + (base * g + qi) * HD, (size_t)g * HD, p.part_ml + (base * g + qi) * 2,
-                   (size_t)g * 2, nch, p.out + ((size_t)b * p.num_q_heads + h * g + qi) * HD, smem_f);
+  // ticket: the CTA that completes the set of chunk records merges them
+  __syncthreads();  // every record write of this CTA is issued
+  if (tid == 0) {
+    __threadfence();
+    int32_t* tk = p.tickets + (size_t)b * p.num_kv_heads + h;
+    const int old = atomicAdd(tk, 1);
+    const int last = old == nch - 1;
+    if (last) *tk = 0;  // every chunk has arrived: ready for the next call
+    last_s = last;
+  }
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  merge_records<HD, NT>(p, p.records + ((size_t)b * p.num_kv_heads + h) * p.chunks * p.rec_floats,
+                        nch, out_bh, kt, Lay::kMergeBytes, mrun_s, lrun_s, corr_s);
 }
 
 struct DraftPlan {
-  int chunks;
-  size_t off_ml, ws_bytes;
+  int chunks, rec_floats;
+  size_t off_rec, ws_bytes;
 };
 
 bool make_draft_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim, int cap,
@@ -358,45 +521,42 @@ bool make_draft_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim,
     return false;
   const int g = num_q_heads / num_kv_heads;
   pl->chunks = ceil_div(cap + max_tail, kChunk);
-  const size_t o_bytes = (size_t)batch * num_kv_heads * pl->chunks * g * head_dim * 4;
-  const size_t ml_bytes = (size_t)batch * num_kv_heads * pl->chunks * g * 2 * 4;
-  pl->off_ml = align_up(o_bytes, 256);
-  pl->ws_bytes = pl->off_ml + align_up(ml_bytes, 256);
+  pl->rec_floats = kRecHead + g * head_dim;
+  pl->off_rec = align_up((size_t)batch * num_kv_heads * 4, 256);
+  pl->ws_bytes =
+      pl->off_rec + align_up((size_t)batch * num_kv_heads * pl->chunks * pl->rec_floats * 4, 256);
   return true;
 }
 
-template <int HD>
-cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream) {
+template <int HD, bool SLOTS>
+cudaError_t launch_draft_impl(const DraftParams& p, cudaStream_t stream) {
+  using Lay = DraftLayout<HD, kChunk>;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_draft_kernel<HD>,
+    cudaError_t e = cudaFuncSetAttribute(sparse_draft_kernel<HD, kChunk, SLOTS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)DraftLayout<HD>::kBytes);
+                                         (int)Lay::bytes(SLOTS));
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t ccfg = {};
-  ccfg.gridDim = dim3(p.chunks, p.num_kv_heads, p.batch);
-  ccfg.blockDim = dim3(kDraftThreads, 1, 1);
-  ccfg.dynamicSmemBytes = DraftLayout<HD>::kBytes;
-  ccfg.stream = stream;
-  ccfg.attrs = pdl;
-  ccfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&ccfg, sparse_draft_kernel<HD>, p);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.group, p.num_kv_heads, p.batch);
-  cfg.blockDim = dim3(kMergeThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = dim3(p.chunks, p.num_kv_heads, p.batch);
+  cfg.blockDim = dim3(Lay::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Lay::bytes(SLOTS);
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sparse_draft_merge_kernel<HD>, p);
+  return cudaLaunchKernelEx(&cfg, sparse_draft_kernel<HD, kChunk, SLOTS>, p);
+}
+
+template <int HD>
+cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream) {
+  return p.slots ? launch_draft_impl<HD, true>(p, stream) : launch_draft_impl<HD, false>(p, stream);
 }
 
 }  // namespace
@@ -412,12 +572,13 @@ extern "C" size_t vg_sparse_draft_workspace_bytes(int batch, int num_q_heads, in
 }
 
 extern "C" vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void* q,
-                                               const int32_t* indices, const int32_t* counts,
-                                               int per_head, int cap, const int32_t* tail_start,
-                                               const int32_t* cur_len, int batch, int num_q_heads,
-                                               int max_tail, float softmax_scale, void* out,
-                                               void* workspace, size_t workspace_bytes,
-                                               int32_t* error_flag, cudaStream_t stream) {
+                                               const int32_t* indices, const int32_t* slots,
+                                               const int32_t* counts, int per_head, int cap,
+                                               const int32_t* tail_start, const int32_t* cur_len,
+                                               int batch, int num_q_heads, int max_tail,
+                                               float softmax_scale, void* out, void* workspace,
+                                               size_t workspace_bytes, int32_t* error_flag,
+                                               cudaStream_t stream) {
   vg_status st = check_paged_kv(kv);
   if (st != VG_OK) return st;
   if (!q || !counts || !tail_start || !cur_len || !out || batch <= 0 || num_q_heads <= 0 ||
@@ -427,10 +588,10 @@ extern "C" vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void
   if (num_q_heads % kv->num_kv_heads) return VG_ERR_INVALID_ARGUMENT;
   const int g = num_q_heads / kv->num_kv_heads;
   if (g > 8) return VG_ERR_UNSUPPORTED;
+  if ((long long)cap + max_tail > kMaxEntries) return VG_ERR_UNSUPPORTED;
   DraftPlan pl;
   if (!make_draft_plan(batch, num_q_heads, kv->num_kv_heads, kv->head_dim, cap, max_tail, &pl))
     return VG_ERR_INVALID_ARGUMENT;
-  if (pl.chunks > kMaxChunks) return VG_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < pl.ws_bytes) return VG_ERR_WORKSPACE_TOO_SMALL;
   DraftParams p;
   p.k_pages = static_cast<const __nv_bfloat16*>(kv->k_pages);
@@ -438,13 +599,14 @@ extern "C" vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void
   p.page_table = kv->page_table;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.indices = indices;
+  p.slots = cap > 0 ? slots : nullptr;
   p.counts = counts;
   p.tail_start = tail_start;
   p.cur_len = cur_len;
   p.out = static_cast<__nv_bfloat16*>(out);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.part_o = reinterpret_cast<float*>(ws);
-  p.part_ml = reinterpret_cast<float*>(ws + pl.off_ml);
+  p.tickets = reinterpret_cast<int32_t*>(ws);
+  p.records = reinterpret_cast<float*>(ws + pl.off_rec);
   p.error_flag = error_flag;
   p.batch = batch;
   p.num_q_heads = num_q_heads;
@@ -456,7 +618,7 @@ extern "C" vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void
   p.num_pages = kv->num_pages;
   p.max_pages_per_seq = kv->max_pages_per_seq;
   p.chunks = pl.chunks;
-  p.pt_cap = kPtMax;
+  p.rec_floats = pl.rec_floats;
   p.scale_log2 = softmax_scale * kLog2e;
   const cudaError_t e = kv->head_dim == 128 ? launch_draft<128>(p, stream)
                                              : launch_draft<64>(p, stream);

@@ -11,7 +11,7 @@
 //    accumulators in tensor memory, M padded to 128), so every K/V page is
 //    read from HBM once per KV head.  Row order in M: [row 0 of each
 //    head][row k of each head][rows 1..k-1].
-//  * A producer warp streams 64-position tiles (4 pages) of K and V into a
+//  * A producer warp streams 128-position tiles (8 pages) of K and V into a
 //    shared-memory ring with 4-D TMA loads (128-byte swizzle, evict-first L2
 //    policy); the swizzled tiles are the tensor cores' K-major (K) and
 //    MN-major (V) B operands as they land.  Q and P, the A operands, live in
@@ -24,7 +24,7 @@
 //    every wait is bounded.
 //  * Softmax warps hold one packed row per lane (tcgen05.ld), so row maxima
 //    and sums need no shuffles; the exponent reference moves only when a row
-//    maximum grows by more than 2^8, and O is then rescaled in TMEM.  P goes
+//    maximum grows by more than 2^32, and O is then rescaled in TMEM.  P goes
 //    back to tensor memory as bf16 pairs.
 //  * Capture epilogue (from the softmax warps' registers): the Collect-2 rows
 //    or their per-KV-head sum in a fixed order, or the Collect-All column
@@ -1232,6 +1232,11 @@ extern "C" vg_status vg_verify_attention_noalloc(const vg_paged_kv* kv, const vo
                         num_splits, &pl))
     return VG_ERR_INVALID_ARGUMENT;
   if (pl.ws_bytes > kNoAllocScratchBytes) return VG_ERR_WORKSPACE_TOO_SMALL;
+  // the scratch array used is the current device's: the stream must belong to it
+  int cur = -1, sdev = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(stream, &sdev) != cudaSuccess)
+    return VG_ERR_LAUNCH;
+  if (cur != sdev) return VG_ERR_INVALID_ARGUMENT;
   uint8_t* scratch = static_cast<uint8_t*>(noalloc_scratch_on_current_device());
   if (!scratch) return VG_ERR_LAUNCH;
   // The array keeps the previous call's contents; nothing in it has to start

@@ -122,6 +122,12 @@ class DecodeStack:
                         for _ in range(s.layers)]
         self.counts = [torch.zeros(B, self.rows, dtype=torch.int32, device=dev)
                        for _ in range(s.layers)]
+        # cache slots of the selections (written by the selector); a forced
+        # selection replaces the positions, so the drafts then translate them
+        # through the page table instead
+        self.slots = None if force_selection is not None else [
+            torch.full((B, self.rows, self.cap), -1, dtype=torch.int32, device=dev)
+            for _ in range(s.layers)]
         self.max_tail = 2 * s.n_drafts + 1
         self.ws_verify = {r: vg.zero_workspace(
             vg.verify_workspace_bytes(B, r, Hq, Hkv, d, s.max_prefix), dev) for r in (1, self.R)}
@@ -178,7 +184,8 @@ class DecodeStack:
         self._timed("select", vg.select_kv, self.capture, vg.CAPTURE_GROUP_SUM, self.lens,
                     s.num_q_heads, s.num_kv_heads, s.max_prefix, s.top_k, s.n_sink, s.n_recent,
                     s.per_head, self.indices[l], self.counts[l], self.flag,
-                    workspace=self.ws_select)
+                    workspace=self.ws_select, kv=self.kv[l],
+                    slots=None if self.slots is None else self.slots[l])
         return out
 
     def _forced(self, kind, l):
@@ -223,7 +230,8 @@ class DecodeStack:
                                   device=self.device)
                 self._timed("draft", vg.sparse_draft_attention, self.kv[l], q, self.indices[l],
                             self.counts[l], s.per_head, self.tail_start, cur, self.max_tail,
-                            s.softmax_scale, out, self.ws_draft, self.flag)
+                            s.softmax_scale, out, self.ws_draft, self.flag,
+                            slots=None if self.slots is None else self.slots[l])
                 if self.record:
                     self.record("draft", l, dict(out=out, t=t))
                 x = x + out.double().reshape(B, -1)
@@ -245,6 +253,15 @@ class DecodeStack:
         self.lens = self.lens + (a_dev + 1).to(torch.int32)
         self.e = _rms(X[torch.arange(B, device=self.device), a_dev])
         self.iteration += 1
+
+    def launches_per_iteration(self) -> int:
+        """Kernels per layer and draft/verify iteration: k drafts, the verify
+        (+ split merge) and the selection."""
+        from .step import select_launches
+        s = self.spec
+        merge = 1 if self.ws_verify[self.R].numel() > 1 else 0
+        return s.n_drafts + 1 + merge + select_launches(vg.CAPTURE_GROUP_SUM, s.per_head,
+                                                        s.num_kv_heads, s.max_prefix)
 
     def run(self, iterations: Optional[int] = None):
         self.seed_selection()

@@ -35,6 +35,9 @@ class DecodeStep:
     ws_select: torch.Tensor
     error_flag: torch.Tensor
     num_splits: int = 0
+    # cache slots written by the selector beside the indices (None: the draft
+    # kernel translates positions through the page table itself)
+    slots: Optional[torch.Tensor] = None
     extra: dict = field(default_factory=dict)
     # The step's inputs (q_verify, draft_q) and results (out_verify,
     # out_draft; indices, counts) are views into three flat buffers, so that a
@@ -45,7 +48,7 @@ class DecodeStep:
 
     @classmethod
     def create(cls, inp: Inputs, device="cuda", capture_mode=vg.CAPTURE_GROUP_SUM,
-               per_head: Optional[bool] = None, num_splits=0):
+               per_head: Optional[bool] = None, num_splits=0, use_slots=True):
         s = inp.spec
         dev = torch.device(device)
         per_head = s.per_head if per_head is None else per_head
@@ -78,6 +81,7 @@ class DecodeStep:
         io_sel = torch.zeros(ni + B * rows, dtype=torch.int32, device=dev)
         indices = io_sel[:ni].view(B, rows, cap)
         indices.fill_(-7)
+        slots = torch.full((B, rows, cap), -7, dtype=torch.int32, device=dev) if use_slots else None
         return cls(spec=s, device=dev, kv=kv, q_verify=q_verify, draft_q=draft_q[:k] if k else draft_q[:0],
                    prefix_lens=prefix, capture_mode=capture_mode, per_head=per_head,
                    capture=capture, out_verify=io_out[:nv].view(B, R, Hq, d),
@@ -85,7 +89,7 @@ class DecodeStep:
                    out_draft=io_out[nv:].view(max(k, 1), B, Hq, d),
                    tail_start=prefix.clone(), cur_len=cur.contiguous(), ws_verify=wsv,
                    ws_draft=wsd, ws_select=wss, error_flag=torch.zeros(1, dtype=torch.int32, device=dev),
-                   num_splits=num_splits, io_in=io_in, io_out=io_out, io_sel=io_sel)
+                   num_splits=num_splits, slots=slots, io_in=io_in, io_out=io_out, io_sel=io_sel)
 
     @property
     def max_tail(self):
@@ -103,6 +107,8 @@ class DecodeStep:
         sp, st = self.spec, ctypes.c_void_p(s.cuda_stream)
         kvs = self.extra.setdefault("kv_struct", self.kv.struct())
         B, R, Hq, d = self.q_verify.shape
+        slots = None if self.slots is None else p(self.slots)
+        kv_arg = None if self.slots is None else ctypes.byref(kvs)
         if kind == "verify":
             a = (ctypes.byref(kvs), p(self.q_verify), p(self.prefix_lens), B, R, Hq,
                  sp.max_prefix, ctypes.c_float(sp.softmax_scale), p(self.out_verify),
@@ -111,15 +117,15 @@ class DecodeStep:
         elif kind == "select" and self.capture_mode == vg.CAPTURE_ALL_ROWS:
             a = (p(self.capture), R, p(self.prefix_lens), B, Hq, sp.num_kv_heads,
                  sp.max_prefix, sp.top_k, sp.n_sink, sp.n_recent, int(self.per_head),
-                 p(self.indices), p(self.counts), self.indices.shape[-1], p(self.ws_select),
-                 self.ws_select.numel(), p(self.error_flag), st)
+                 p(self.indices), p(self.counts), self.indices.shape[-1], kv_arg, slots,
+                 p(self.ws_select), self.ws_select.numel(), p(self.error_flag), st)
         elif kind == "select":
             a = (p(self.capture), self.capture_mode, p(self.prefix_lens), B, Hq, sp.num_kv_heads,
                  sp.max_prefix, sp.top_k, sp.n_sink, sp.n_recent, int(self.per_head),
-                 p(self.indices), p(self.counts), self.indices.shape[-1], p(self.ws_select),
-                 self.ws_select.numel(), p(self.error_flag), st)
+                 p(self.indices), p(self.counts), self.indices.shape[-1], kv_arg, slots,
+                 p(self.ws_select), self.ws_select.numel(), p(self.error_flag), st)
         else:
-            a = (ctypes.byref(kvs), p(self.draft_q[t - 1]), p(self.indices), p(self.counts),
+            a = (ctypes.byref(kvs), p(self.draft_q[t - 1]), p(self.indices), slots, p(self.counts),
                  int(self.per_head), self.indices.shape[-1], p(self.tail_start),
                  p(self.cur_len[t - 1]), B, Hq, self.max_tail, ctypes.c_float(sp.softmax_scale),
                  p(self.out_draft[t - 1]), p(self.ws_draft), self.ws_draft.numel(),
@@ -149,7 +155,24 @@ class DecodeStep:
             self.draft(t, stream)
 
     def launches_per_step(self) -> int:
-        """Kernels of one step: verify (+ its split merge), select (score pass
-        and cluster select), k drafts (each a chunk kernel plus its merge)."""
+        """Kernels of one step: verify (+ its split merge when it has more
+        than one split), the selection's kernels, one kernel per draft step."""
         merge = 1 if self.ws_verify.numel() > 1 else 0
-        return 3 + merge + 2 * self.spec.n_drafts  # select = score pass + cluster select
+        sp = self.spec
+        return (1 + merge + select_launches(self.capture_mode, self.per_head, sp.num_kv_heads,
+                                            sp.max_prefix) + sp.n_drafts)
+
+
+def select_launches(capture_mode, per_head, num_kv_heads, max_prefix) -> int:
+    """Kernels vg_select_kv launches, restating the library's rule: one
+    cluster of up to 16 CTAs per selection row takes slices of at least 2048
+    positions; the cluster forms the score keys itself for per-KV-head sum
+    captures when a CTA has at most 16384 capture loads, otherwise a score
+    kernel runs first."""
+    c = 1
+    while c < 16 and -(-max_prefix // c) > 2048:
+        c *= 2
+    slice_ = (-(-max_prefix // c) + 3) // 4 * 4
+    fused = capture_mode in (vg.CAPTURE_GROUP_SUM, vg.CAPTURE_ALL_SUM) and \
+        (1 if per_head else num_kv_heads) * slice_ <= 16384
+    return 1 if fused else 2

@@ -63,12 +63,12 @@ def _load():
                                       vp, sz, vp, vp]),
         "vg_select_workspace_bytes": (sz, [i32, i32, i32, i32]),
         "vg_select_kv_weights": (i32, [vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp,
-                                       vp, i32, vp, sz, vp, vp]),
+                                       vp, i32, kvp, vp, vp, sz, vp, vp]),
         "vg_select_kv": (i32, [vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, i32,
-                               vp, sz, vp, vp]),
+                               kvp, vp, vp, sz, vp, vp]),
         "vg_sparse_draft_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
-        "vg_sparse_draft_attention": (i32, [kvp, vp, vp, vp, i32, i32, vp, vp, i32, i32, i32, f32,
-                                            vp, vp, sz, vp, vp]),
+        "vg_sparse_draft_attention": (i32, [kvp, vp, vp, vp, vp, i32, i32, vp, vp, i32, i32, i32,
+                                            f32, vp, vp, sz, vp, vp]),
         "vg_verify_noalloc_scratch_bytes": (sz, []),
         "vg_verify_attention_noalloc": (i32, [kvp, vp, vp, i32, i32, i32, i32, f32, vp, i32, vp,
                                               i32, vp, vp]),
@@ -207,20 +207,30 @@ def select_workspace_bytes(batch, num_kv_heads, max_prefix, per_head) -> int:
     return int(_lib.vg_select_workspace_bytes(batch, num_kv_heads, max_prefix, int(bool(per_head))))
 
 
+def _kv_arg(kv, slots):
+    if slots is None:
+        return None, None
+    assert kv is not None, "slots need the paged cache whose page table they translate"
+    return kv.struct(), slots
+
+
 def select_kv(capture, capture_mode, prefix_lens, num_q_heads, num_kv_heads, max_prefix, top_k,
               n_sink, n_recent, per_head, indices, counts, error_flag=None, stream=None,
-              workspace=None):
-    """vg_select_kv.  indices int32 [B][rows][cap], counts int32 [B][rows].
-    workspace: uint8 device tensor of select_workspace_bytes() (allocated here
-    when not given)."""
+              workspace=None, kv=None, slots=None):
+    """vg_select_kv.  indices int32 [B][rows][cap], counts int32 [B][rows];
+    slots (optional, with kv) int32 like indices: the cache slots of the kept
+    positions.  workspace: uint8 device tensor of select_workspace_bytes()
+    (allocated here when not given)."""
     B = prefix_lens.shape[0]
     cap = indices.shape[-1]
     if workspace is None:
         workspace = zero_workspace(select_workspace_bytes(B, num_kv_heads, max_prefix, per_head),
                                    indices.device)
+    st, slots = _kv_arg(kv, slots)
     s = _lib.vg_select_kv(_ptr(capture), int(capture_mode), _ptr(prefix_lens), B, num_q_heads,
                           num_kv_heads, int(max_prefix), int(top_k), int(n_sink), int(n_recent),
-                          int(bool(per_head)), _ptr(indices), _ptr(counts), cap, _ptr(workspace),
+                          int(bool(per_head)), _ptr(indices), _ptr(counts), cap,
+                          None if st is None else ctypes.byref(st), _ptr(slots), _ptr(workspace),
                           workspace.numel(), _ptr(error_flag), _stream(stream))
     _check("vg_select_kv", s)
     return indices, counts
@@ -233,7 +243,7 @@ def all_rows_capture_floats(batch, num_q_heads, n_rows, max_prefix) -> int:
 
 def select_kv_weights(capture, n_rows, prefix_lens, num_q_heads, num_kv_heads, max_prefix,
                       top_k, n_sink, n_recent, per_head, indices, counts, error_flag=None,
-                      stream=None, workspace=None):
+                      stream=None, workspace=None, kv=None, slots=None):
     """vg_select_kv_weights: selection by the post-softmax weights of the
     n_rows captured rows (capture from VG_CAPTURE_ALL_ROWS)."""
     B = prefix_lens.shape[0]
@@ -241,10 +251,12 @@ def select_kv_weights(capture, n_rows, prefix_lens, num_q_heads, num_kv_heads, m
     if workspace is None:
         workspace = zero_workspace(select_workspace_bytes(B, num_kv_heads, max_prefix, per_head),
                                    indices.device)
+    st, slots = _kv_arg(kv, slots)
     s = _lib.vg_select_kv_weights(_ptr(capture), int(n_rows), _ptr(prefix_lens), B, num_q_heads,
                                   num_kv_heads, int(max_prefix), int(top_k), int(n_sink),
                                   int(n_recent), int(bool(per_head)), _ptr(indices), _ptr(counts),
-                                  cap, _ptr(workspace), workspace.numel(), _ptr(error_flag),
+                                  cap, None if st is None else ctypes.byref(st), _ptr(slots),
+                                  _ptr(workspace), workspace.numel(), _ptr(error_flag),
                                   _stream(stream))
     _check("vg_select_kv_weights", s)
     return indices, counts
@@ -258,13 +270,16 @@ def sparse_draft_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, cap
 
 def sparse_draft_attention(kv: PagedKV, q, indices, counts, per_head, tail_start, cur_len,
                            max_tail, softmax_scale, out, workspace=None, error_flag=None,
-                           stream=None):
-    """vg_sparse_draft_attention.  q [B][Hq][d] bf16."""
+                           stream=None, slots=None):
+    """vg_sparse_draft_attention.  q [B][Hq][d] bf16; slots (optional) as
+    written by select_kv beside the indices.  The workspace must be
+    zero-filled before its first use (zero_workspace does that)."""
     B, Hq, _ = q.shape
     st = kv.struct()
     cap = indices.shape[-1]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    s = _lib.vg_sparse_draft_attention(ctypes.byref(st), _ptr(q), _ptr(indices), _ptr(counts),
+    s = _lib.vg_sparse_draft_attention(ctypes.byref(st), _ptr(q), _ptr(indices), _ptr(slots),
+                                       _ptr(counts),
                                        int(bool(per_head)), cap, _ptr(tail_start), _ptr(cur_len),
                                        B, Hq, int(max_tail), float(softmax_scale), _ptr(out),
                                        _ptr(workspace), ws_bytes, _ptr(error_flag),
@@ -274,7 +289,7 @@ def sparse_draft_attention(kv: PagedKV, q, indices, counts, per_head, tail_start
 
 
 def zero_workspace(nbytes: int, device) -> torch.Tensor:
-    """A zero-filled byte workspace.  No call needs its workspace initialised
-    (every partial is written before it is read); zeros only keep a fresh
-    buffer free of stale bytes."""
+    """A zero-filled byte workspace.  The sparse-draft workspace needs it (its
+    completion counters start at zero); for the others zeros only keep a
+    fresh buffer free of stale bytes."""
     return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)

@@ -204,10 +204,11 @@ def check_select_end_to_end(st, inp, rows64):
     return worst
 
 
-def check_drafts(st, inp, oracle_sel, pairs=None, steps=None):
+def check_drafts(st, inp, oracle_sel, pairs=None, steps=None, min_pairs=1):
     """GPU drafts (run on the GPU's own selection) vs the oracle's drafts on
     the oracle's selection, for the (sequence, KV head) pairs whose two
-    selections are identical.  Returns the number of pairs compared."""
+    selections are identical; at least `min_pairs` pairs must be compared.
+    Returns the number of pairs compared."""
     s = inp.spec
     _, k, v = dense64(inp)
     g = s.group
@@ -225,6 +226,7 @@ def check_drafts(st, inp, oracle_sel, pairs=None, steps=None):
                                            [v[b][h:h + 1]], sel, False, [s.prefix_lens[b]],
                                            [s.prefix_lens[b] + t], s.softmax_scale)
             assert_close_out(got[b, h * g:(h + 1) * g], ref[0], f"draft t={t} b={b} h={h}")
+    assert len(same) >= min_pairs, f"only {len(same)} of {len(pairs)} pairs had the oracle's selection"
     return len(same)
 
 
@@ -236,6 +238,8 @@ def check_drafts_synthetic(st, inp, per_head, seed=9, pairs=None, steps=None):
     idx, cnt = make_selection(s, per_head, seed)
     st.indices.copy_(idx.to(st.indices.device))
     st.counts.copy_(cnt.to(st.counts.device))
+    if st.slots is not None:
+        st.slots.copy_(cache_slots(idx, cnt, inp.page_table).to(st.slots.device))
     steps = steps or list(range(1, s.n_drafts + 1))
     for t in steps:
         st.draft(t)
@@ -254,6 +258,42 @@ def check_drafts_synthetic(st, inp, per_head, seed=9, pairs=None, steps=None):
                                            [s.prefix_lens[b]], [s.prefix_lens[b] + t],
                                            s.softmax_scale)
             assert_close_out(got[b, h * g:(h + 1) * g], ref[0], f"draft t={t} b={b} h={h}")
+
+
+def cache_slots(idx, cnt, page_table):
+    """Cache slots of index lists (page-table layout, not method arithmetic):
+    page_table[b][p // 16] * 16 + p % 16 for every listed position p, -1
+    past the count."""
+    idx = idx.long()
+    B, rows, cap = idx.shape
+    pos = idx.clamp(min=0)
+    phys = torch.gather(page_table.long()[:, None, :].expand(B, rows, -1), 2, pos // 16)
+    out = phys * 16 + pos % 16
+    live = torch.arange(cap)[None, None, :] < cnt.long()[:, :, None]
+    return torch.where(live, out, torch.full_like(out, -1)).to(torch.int32)
+
+
+def check_slots(st, inp):
+    """The cache slots the selector wrote beside its positions equal the page
+    table's translation of those positions, bit for bit (-1 past the count)."""
+    if st.slots is None:
+        return
+    want = cache_slots(st.indices.cpu(), st.counts.cpu(), inp.page_table)
+    got = st.slots.cpu()
+    assert torch.equal(got, want), f"{(got != want).sum().item()} cache slots differ"
+
+
+def draft_counter_bytes(st):
+    """Bytes of completion counters at the start of the sparse-draft
+    workspace (they must stay zero between calls)."""
+    B, Hkv = st.spec.batch, st.spec.num_kv_heads
+    return (B * Hkv * 4 + 255) // 256 * 256
+
+
+def poison_draft_workspace(st):
+    """NaN bit patterns over every chunk record of the draft workspace; the
+    completion counters are left at zero."""
+    st.ws_draft[draft_counter_bytes(st):].fill_(0xFF)
 
 
 def flag(st):

@@ -93,27 +93,33 @@ def test_host_argument_checks_without_gpu():
     assert L.vg_verify_attention(ctypes.byref(kv2), fake, fake, 1, 6, 32, 5000, 0.1, fake, 1, fake,
                                  24, None, 0, None, None) == 3
     # select: cap too small, bad mode, non-divisible heads
-    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 50, None, 0,
-                          None, None) == 1
-    assert L.vg_select_kv(fake, 0, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None, 0,
-                          None, None) == 1
-    assert L.vg_select_kv(fake, 1, fake, 1, 30, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None, 0,
-                          None, None) == 1
-    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 300000, 100, 4, 16, 0, fake, fake, 200, None, 0,
-                          None, None) == 2
+    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 50, None,
+                          None, None, 0, None, None) == 1
+    assert L.vg_select_kv(fake, 0, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None,
+                          None, None, 0, None, None) == 1
+    assert L.vg_select_kv(fake, 1, fake, 1, 30, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None,
+                          None, None, 0, None, None) == 1
+    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 300000, 100, 4, 16, 0, fake, fake, 200, None,
+                          None, None, 0, None, None) == 2
     # select: the score-key workspace is missing or too small
     assert L.vg_select_workspace_bytes(1, 8, 5000, 0) >= 5000 * 4
-    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None, 0,
-                          None, None) == 3
-    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 1, fake, fake, 200, fake,
-                          5000 * 4, None, None) == 3
-    # sparse draft: g > 8; a list longer than 1024 chunks of 64; missing workspace
-    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 200, fake, fake, 1,
-                                       80, 5, 0.1, fake, None, 0, None, None) == 2
+    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None,
+                          None, None, 0, None, None) == 3
+    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 1, fake, fake, 200, None,
+                          None, fake, 5000 * 4, None, None) == 3
+    # select: slots without the cache, or a page table too short for max_prefix
+    ws = L.vg_select_workspace_bytes(1, 8, 5000, 0)
+    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None,
+                          fake, fake, ws, None, None) == 1
+    assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 200,
+                          ctypes.byref(kv), fake, fake, ws, None, None) == 1
+    # sparse draft: g > 8; a list longer than 65536 entries; missing workspace
+    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, None, fake, 0, 200, fake,
+                                       fake, 1, 80, 5, 0.1, fake, None, 0, None, None) == 2
     assert L.vg_sparse_draft_workspace_bytes(1, 32, 8, 128, 200, 5) > 0
-    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 70000, fake, fake, 1,
-                                       32, 5, 0.1, fake, fake, 1 << 30, None, None) == 2
-    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, 0, 200, fake, fake, 1,
-                                       32, 5, 0.1, fake, None, 0, None, None) == 3
-    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, None, fake, 0, 200, fake, fake, 1,
-                                       32, 5, 0.1, fake, None, 0, None, None) == 1
+    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, fake, fake, 0, 70000, fake,
+                                       fake, 1, 32, 5, 0.1, fake, fake, 1 << 30, None, None) == 2
+    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, fake, None, fake, 0, 200, fake,
+                                       fake, 1, 32, 5, 0.1, fake, None, 0, None, None) == 3
+    assert L.vg_sparse_draft_attention(ctypes.byref(kv), fake, None, None, fake, 0, 200, fake,
+                                       fake, 1, 32, 5, 0.1, fake, None, 0, None, None) == 1

@@ -58,8 +58,30 @@ def test_small_step(name, mode, per_head):
     rows64 = P.oracle_rows(inp)
     P.check_capture(st, inp, rows64)
     P.check_select_end_to_end(st, inp, rows64)
+    P.check_slots(st, inp)
     P.check_drafts(st, inp, P.oracle_sets(inp, rows64, per_head))
     P.check_select_synthetic(spec, mode, per_head)
+    P.check_drafts_synthetic(st, inp, per_head)
+
+
+@pytest.mark.parametrize("name", ["base", "d64", "g8", "k0", "pages_shuffled", "short",
+                                  "many_pairs", "long_list"])
+@pytest.mark.parametrize("per_head", [False, True])
+def test_draft_without_slots(name, per_head):
+    """Drafts on positions alone (no cache slots: the kernel stages the page
+    table itself) against the oracle, on the GPU's selection and on
+    generator-made index lists."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.step import DecodeStep
+    from self_speculative_sparse_vg_gb300.workloads import make_inputs, small_spec
+    spec = small_spec(**SMALL[name])
+    inp = make_inputs(spec)
+    st = DecodeStep.create(inp, "cuda", per_head=per_head, use_slots=False)
+    st.run()
+    assert P.flag(st) == 0
+    rows64 = P.oracle_rows(inp)
+    P.check_select_end_to_end(st, inp, rows64)
+    P.check_drafts(st, inp, P.oracle_sets(inp, rows64, per_head))
     P.check_drafts_synthetic(st, inp, per_head)
 
 
@@ -176,7 +198,7 @@ def test_poisoned_workspace_and_repeat():
     ref_v, ref_d = st.out_verify.clone(), st.out_draft.clone()
     assert st.ws_verify.numel() > 1
     st.ws_verify.fill_(0xFF)   # NaN bit patterns in every partial
-    st.ws_draft.fill_(0xFF)
+    P.poison_draft_workspace(st)
     for _ in range(3):
         st.run()
     assert P.flag(st) == 0
@@ -198,7 +220,7 @@ def test_draft_graph_replay_eager_and_empty_list(kw):
     st = DecodeStep.create(inp, "cuda")
     st.run()
     ref = st.out_draft.clone()
-    st.ws_draft.fill_(0xFF)   # NaN bit patterns in every partial
+    P.poison_draft_workspace(st)   # NaN bit patterns in every chunk record
     k = st.spec.n_drafts
     graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -265,6 +287,18 @@ def test_device_errors_flag_and_skip():
     st.kv.page_table.copy_(inp.page_table.cuda())
     st.run()
     assert P.flag(st) == 0
+    good = st.slots[0, 0, 5].item()
+    st.slots[0, 0, 5] = (good & ~15) | ((good + 1) & 15)      # slot of another offset in its page
+    st.draft(1)
+    assert P.flag(st) == V.DEVERR_INDEX
+    st.error_flag.zero_()
+    st.slots[0, 0, 5] = (st.kv.k_pages.shape[0] + 3) * 16 + (good & 15)  # page outside the pool
+    st.draft(1)
+    assert P.flag(st) == V.DEVERR_PAGE
+    st.error_flag.zero_()
+    st.slots[0, 0, 5] = good
+    st.draft(1)
+    assert P.flag(st) == 0
     st.indices[0, 0, 0] = int(st.prefix_lens[0]) + 3          # index beyond the prefix
     st.draft(1)
     assert P.flag(st) & V.DEVERR_INDEX
@@ -296,12 +330,13 @@ def test_full_size_workload(name):
         inp, st = _run(spec, capture_mode=mode, per_head=per_head)
         if name == "tiny_d64_2k":
             pairs = None
-        else:
-            pairs = [(0, 0), (spec.batch - 1, spec.num_kv_heads - 1)]
+        else:  # every KV head of the first and of the last sequence
+            pairs = sorted({(b, h) for b in (0, spec.batch - 1) for h in range(spec.num_kv_heads)})
         P.check_verify(st, inp, pairs)
         rows64 = P.oracle_rows(inp)
         P.check_capture(st, inp, rows64)
         P.check_select_end_to_end(st, inp, rows64)
+        P.check_slots(st, inp)
         osets = P.oracle_sets(inp, rows64, per_head, capture_mode=mode)
         P.check_drafts(st, inp, osets, pairs=pairs, steps=[1, spec.n_drafts])
         if name == "tiny_d64_2k":
