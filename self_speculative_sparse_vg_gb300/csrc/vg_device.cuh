@@ -29,6 +29,16 @@ __device__ __forceinline__ void flag_error(int32_t* flag, int code) {
   if (flag) atomicOr(flag, code);
 }
 
+// Atomic add with acquire-release semantics at GPU scope: the caller's
+// earlier writes (and, after a CTA barrier, its CTA's) are visible to a
+// thread that observes the new value, and writes observed through the old
+// value are visible to the caller afterwards.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -142,6 +152,20 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
       "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Four rows of a 2-D tiled tensor map (box = columns x 1 row) gathered into
+// shared memory: the rows land one after another, each box-width bytes, with
+// the map's swizzle.  Row coordinates past the map's extent read zeros;
+// completion counted on `bar`.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
       : "memory");
 }
 
