@@ -95,7 +95,7 @@ enum {
   VG_DEVERR_PAGE = 1,     /* page-table entry outside [0, num_pages)          */
   VG_DEVERR_INDEX = 2,    /* selected index outside [0, tail_start)           */
   VG_DEVERR_COUNT = 4,    /* selected count outside [0, cap]                  */
-  VG_DEVERR_TIMEOUT = 8,  /* a bounded pipeline wait gave up                  */
+  VG_DEVERR_TIMEOUT = 8,  /* a pipeline wait outlasted its bound (see below)   */
   VG_DEVERR_LENGTH = 16   /* a device length exceeds its host-side bound      */
 };
 
@@ -335,6 +335,22 @@ vg_status vg_verify_attention_noalloc(const vg_paged_kv* kv, const void* q,
                                       int num_q_heads, int max_prefix, float softmax_scale,
                                       void* out, int capture_mode, float* capture,
                                       int num_splits, int32_t* error_flag, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Failure detection: the bound on pipeline waits (host).
+ * Every wait of a kernel on a copy, a tensor-core operation or another warp
+ * is bounded.  A wait longer than `limit_ns` ORs VG_DEVERR_TIMEOUT into
+ * *error_flag and goes on waiting, up to 1 s in all; so a short bound
+ * reports slow waits without abandoning work in flight, and the call's
+ * results are still complete.  A wait that outlasts 1 s is abandoned: the
+ * kernel stops issuing work, waits (again at most 1 s) for the copies and
+ * tensor-core operations it already issued, and returns with the flag set;
+ * its outputs are then undefined.
+ *   limit_ns  0 restores the default (1 s).  Takes effect for calls made
+ *             after it returns, on every device; not synchronised with calls
+ *             made concurrently from other host threads.
+ * ------------------------------------------------------------------------- */
+vg_status vg_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Static string for a status code (host). */
 const char* vg_status_string(vg_status status);

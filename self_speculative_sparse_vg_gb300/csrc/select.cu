@@ -53,6 +53,7 @@ struct SelectParams {
   int top_k, n_sink, n_recent, per_head, cap, rows, slice;
   int n_rows;         // VG_CAPTURE_ALL_ROWS: verify rows per head
   size_t lse_offset;  // VG_CAPTURE_ALL_ROWS: floats before the per-row normalisers
+  uint64_t wait_ns;   // a wait longer than this reports VG_DEVERR_TIMEOUT (and goes on)
 };
 
 // Order-preserving map float -> uint32 (larger float -> larger key), -0 as +0.
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
                     mapa_shared(smem_u32(&mb[pass]), dst));
       }
       if (tid < 256) {
-        if (!mbar_wait(&mb[pass], 0)) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+        mbar_wait_checked(&mb[pass], 0, p.wait_ns, p.error_flag);
         uint32_t v[kMaxCluster];
 #pragma unroll
         for (int c = 0; c < kMaxCluster; ++c) v[c] = c < C ? rp[c * 256 + tid] : 0u;
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   // resident until all of them are
   cluster_arrive_release();
   if (tid < 32) {  // lane c takes CTA c's counts; sum over the lower ranks
-    if (!mbar_wait(&mb[4], 0)) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+    mbar_wait_checked(&mb[4], 0, p.wait_ns, p.error_flag);
     int gv = 0, ev = 0;
     if (lane < rank) {
       gv = (int)crecv[lane].x;
@@ -576,6 +577,7 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
   p.n_recent = n_recent;
   p.per_head = per_head ? 1 : 0;
   p.cap = cap;
+  p.wait_ns = wait_report_ns();
   p.rows = per_head ? num_kv_heads : 1;
   p.slice = slice;
   // the cluster forms the keys itself when its CTAs have few loads to issue

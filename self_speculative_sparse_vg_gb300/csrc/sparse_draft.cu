@@ -69,6 +69,7 @@ struct DraftParams {
   int32_t* error_flag;
   int batch, num_q_heads, num_kv_heads, group, per_head, cap, max_tail;
   int num_pages, max_pages_per_seq, segments, cpc, rec_floats;
+  uint64_t wait_ns;        // a wait longer than this reports VG_DEVERR_TIMEOUT (and goes on)
   float scale_log2;
 };
 
@@ -170,13 +171,11 @@ __device__ __forceinline__ void gather_chunk(const DraftParams& p, int row, int*
   }
 }
 
-// Wait for a ring stage; a wait that gives up is reported and waited out
-// once more, so that no load is left writing into shared memory.
+// Wait for a ring stage.  A slow wait is reported and goes on; one that
+// gives up even so is waited out once more (bounded), so that no load is
+// left writing into shared memory when the CTA leaves.
 __device__ __forceinline__ void wait_stage(const DraftParams& p, uint64_t* bar, uint32_t parity) {
-  if (!mbar_wait(bar, parity)) {
-    if (threadIdx.x == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-    mbar_wait(bar, parity);
-  }
+  if (!mbar_wait_checked(bar, parity, p.wait_ns, p.error_flag)) mbar_wait(bar, parity);
 }
 
 // Log-sum-exp merge of the nseg segment records of one (sequence, KV head)
@@ -369,10 +368,7 @@ __global__ void __launch_bounds__(kThreads) sparse_draft_kernel(const DraftParam
   if (!SLOTS) {
     // the page-table copy must land before anything reads it or the CTA
     // leaves; a wait that gives up is reported and waited out once more
-    if (!mbar_wait(&bars[0], 0)) {
-      flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-      mbar_wait(&bars[0], 0);
-    }
+    if (!mbar_wait_checked(&bars[0], 0, p.wait_ns, p.error_flag)) mbar_wait(&bars[0], 0);
   }
   __nv_bfloat16* out_bh = p.out + ((size_t)b * p.num_q_heads + h * g) * HD;
   if (!lengths_ok) {
@@ -716,6 +712,7 @@ extern "C" vg_status vg_sparse_draft_attention(const vg_paged_kv* kv, const void
   p.segments = pl.segments;
   p.cpc = pl.cpc;
   p.rec_floats = pl.rec_floats;
+  p.wait_ns = wait_report_ns();
   p.scale_log2 = softmax_scale * kLog2e;
   const cudaError_t e = kv->head_dim == 128 ? launch_draft<128>(p, stream)
                                              : launch_draft<64>(p, stream);

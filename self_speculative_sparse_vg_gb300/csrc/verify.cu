@@ -61,6 +61,7 @@ struct VerifyParams {
   uint32_t* u_masks;   // [B][u_max] bit i: verify row i selected the page
   int32_t* u_count;    // [B]
   int u_max;
+  uint64_t wait_ns;    // a wait longer than this reports VG_DEVERR_TIMEOUT (and goes on)
   float scale, scale_log2;
 };
 
@@ -120,7 +121,7 @@ struct VerifyLayout {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kCapFloats = 4 * 16 * kCapStride;  // per-warp Collect-2 staging
   static constexpr int kAllFloats = 2 * 4 * kVTile;       // Collect-All partials [slot][warp]
-  static constexpr int kBars = 12;                        // besides the ring's 4 per stage
+  static constexpr int kBars = 13;                        // besides the ring's 4 per stage
   static constexpr int kSliceMax = 1024;                  // sparse: union pages of one split
   static size_t bytes(int stages) {
     return 1024 + (size_t)stages * kStageBytes + (size_t)(kCapFloats + kAllFloats) * 4 +
@@ -129,7 +130,7 @@ struct VerifyLayout {
 };
 
 struct VerifyBars {
-  uint64_t *kfull, *vfull, *kempty, *empty, *s_full, *p_full, *capfull, *capfree;
+  uint64_t *kfull, *vfull, *kempty, *empty, *s_full, *p_full, *capfull, *capfree, *drain;
   int stages;
 };
 
@@ -172,7 +173,7 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
     const int sb = lt & 1, u = lt >> 1;
     const int tile_pos = (t0 + lt) * kVTile;
     const uint32_t sbuf = trow + kSCol + sb * kVTile;
-    if (live && !mbar_wait(&bars.s_full[sb], u & 1)) live = false;
+    if (live && !mbar_wait_checked(&bars.s_full[sb], u & 1, p.wait_ns, p.error_flag)) live = false;
     tc_fence_after();
     const int cpos = tile_pos + col0;  // position of this warp's first column
     const int rem = lim - cpos;        // last attended column of this row among the warp's
@@ -277,13 +278,17 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
       const int cb = c * 2 + slot;  // this copy's handshake barrier of the slot
       float* part = all_s + slot * 4 * kVTile;
       if (wq != 0) {
-        if (lt >= 2 && live && !mbar_wait(&bars.capfree[cb], ((lt >> 1) - 1) & 1)) live = false;
+        if (lt >= 2 && live &&
+            !mbar_wait_checked(&bars.capfree[cb], ((lt >> 1) - 1) & 1, p.wait_ns, p.error_flag))
+          live = false;
 #pragma unroll
         for (int k = 0; k < NCH; ++k) part[warp * kVTile + k * kChunk + lane] = call[k];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.capfull[cb]);
       } else {
-        if (nwc > 1 && live && !mbar_wait(&bars.capfull[cb], (lt >> 1) & 1)) live = false;
+        if (nwc > 1 && live &&
+            !mbar_wait_checked(&bars.capfull[cb], (lt >> 1) & 1, p.wait_ns, p.error_flag))
+          live = false;
         float* dst = p.capture + ((size_t)b * p.num_kv_heads + h) * p.max_prefix + cpos;
 #pragma unroll
         for (int k = 0; k < NCH; ++k) {
@@ -305,7 +310,9 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
       lsum *= corr;
       if (lt > 0) {  // O holds P(0..t-1) V: wait for the last P.V, then scale the row
         const int pst = (lt - 1) % stages;
-        if (live && !mbar_wait(&bars.empty[pst], ((lt - 1) / stages) & 1)) live = false;
+        if (live &&
+            !mbar_wait_checked(&bars.empty[pst], ((lt - 1) / stages) & 1, p.wait_ns, p.error_flag))
+          live = false;
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < HD / 32; ++cc) {
@@ -355,12 +362,10 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars.p_full[sb]);
   }
-  if (!live && lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-
   // -------- epilogue: merge the copies, then this lane's row of O
-  if (ntiles > 0 &&
-      !mbar_wait(&bars.empty[(ntiles - 1) % stages], ((ntiles - 1) / stages) & 1))
-    flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+  if (ntiles > 0)
+    mbar_wait_checked(&bars.empty[(ntiles - 1) % stages], ((ntiles - 1) / stages) & 1, p.wait_ns,
+                      p.error_flag);
   tc_fence_after();
   // scratch in the idle ring, column-major so that a warp's 32 rows are 32
   // consecutive floats: so[copy - 1][d][row], sml[copy - 1][{m, l}][row]
@@ -485,7 +490,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   bars.p_full = bars.s_full + 2;      // P of a buffer written by every softmax warp
   bars.capfull = bars.p_full + 2;     // [copy][slot]: Collect-All partials written
   bars.capfree = bars.capfull + 4;    // [copy][slot]: Collect-All slot read
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars.capfree + 4);
+  bars.drain = bars.capfree + 4;      // every tensor-core operation issued so far done
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars.drain + 1);
 
   // the K/V tensor maps are kernel parameters, independent of earlier
   // kernels: fetch their descriptors before anything else so that the first
@@ -567,6 +573,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
       mbar_init(&bars.capfull[s], nwc > 1 ? nwc - 1 : 1);
       mbar_init(&bars.capfree[s], 1);
     }
+    mbar_init(bars.drain, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(tmem_holder, kTmemCols);
@@ -616,6 +623,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
       // page ids of tiles [4w, 4w + 4) for the window w of the K tile, and of
       // the window before it (V runs one tile behind)
       int id_cur = p.num_pages, id_prev = p.num_pages;
+      int k_armed = 0, v_armed = 0;  // K / V tile loads issued
       for (int kt = 0; kt <= ntiles; ++kt) {
         const int vt = kt - 1;
         const bool new_window = kt < ntiles && (kt & 3) == 0;
@@ -638,12 +646,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
         if (kt < ntiles) {
           const int st = kt % stages;
           int go = 1;
-          if (lane == 0 && kt >= stages) go = mbar_wait(&bars.kempty[st], ((kt / stages) - 1) & 1);
+          if (lane == 0 && kt >= stages)
+            go = mbar_wait_checked(&bars.kempty[st], ((kt / stages) - 1) & 1, p.wait_ns,
+                                   p.error_flag);
           go = __shfl_sync(0xffffffffu, go, 0);
-          if (!go) {
-            if (lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-            break;
-          }
+          if (!go) break;  // the consumer is gone: stop, then drain what is in flight
           const int id = __shfl_sync(0xffffffffu, id_cur, (kt & 3) * 8 + (pi & 7));
           if (lane == 0) mbar_arrive_expect_tx(&bars.kfull[st], kTileBytes);
           __syncwarp();
@@ -651,16 +658,16 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
             tma_load_4d(ring + st * kStageBytes + dh * Lay::kHalfBytes + pi * kPageSize * 128, &tmk,
                         &bars.kfull[st], dh * 64, 0, h, id, pol);
           __syncwarp();
+          ++k_armed;
         }
         if (vt >= 0) {
           const int st = vt % stages;
           int go = 1;
-          if (lane == 0 && vt >= stages) go = mbar_wait(&bars.empty[st], ((vt / stages) - 1) & 1);
+          if (lane == 0 && vt >= stages)
+            go = mbar_wait_checked(&bars.empty[st], ((vt / stages) - 1) & 1, p.wait_ns,
+                                   p.error_flag);
           go = __shfl_sync(0xffffffffu, go, 0);
-          if (!go) {
-            if (lane == 0) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-            break;
-          }
+          if (!go) break;
           const int idv = new_window ? id_prev : id_cur;  // V's tile is in the window before
           const int id = __shfl_sync(0xffffffffu, idv, (vt & 3) * 8 + (pi & 7));
           if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[st], kTileBytes);
@@ -670,8 +677,21 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
                             pi * kPageSize * 128,
                         &tmv, &bars.vfull[st], dh * 64, 0, h, id, pol);
           __syncwarp();
+          ++v_armed;
         }
       }
+      // After a normal run every load has been consumed.  After an abandoned
+      // run, wait (bounded) for the last load armed on every stage, so that no
+      // copy is still writing into shared memory when the CTA leaves.
+      if (lane == 0 && (k_armed < ntiles || v_armed < ntiles)) {
+        for (int s = 0; s < stages; ++s) {
+          if (k_armed > s)
+            mbar_wait(&bars.kfull[s], (((k_armed - 1 - s) / stages)) & 1);
+          if (v_armed > s)
+            mbar_wait(&bars.vfull[s], (((v_armed - 1 - s) / stages)) & 1);
+        }
+      }
+      __syncwarp();
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issue
@@ -682,7 +702,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
       // Issue whichever is ready: S(t) = Q K(t)^T (needs tile t and P(t - 2) V
       // done, which frees its S buffer) or O += P(t) V(t) (needs P(t)).
       int nq = 0, np = 0;
-      bool live = true;
+      bool live = true, reported = false;
       uint64_t last = global_timer_ns();
       while (np < ntiles) {
         bool moved = false;
@@ -724,16 +744,26 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
         }
         if (moved) {
           last = global_timer_ns();
-        } else if (global_timer_ns() - last > kWaitLimitNs) {
-          live = false;
-          break;
+        } else {
+          const uint64_t idle = global_timer_ns() - last;
+          if (!reported && (idle > p.wait_ns || idle > kWaitLimitNs)) {
+            flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+            reported = true;
+          }
+          if (idle > kWaitLimitNs) {
+            live = false;
+            break;
+          }
         }
       }
       // the last P.V has finished before the tensor memory is released
-      if (live &&
-          !mbar_wait(&bars.empty[(ntiles - 1) % stages], ((ntiles - 1) / stages) & 1))
+      if (live && !mbar_wait_checked(&bars.empty[(ntiles - 1) % stages],
+                                     ((ntiles - 1) / stages) & 1, p.wait_ns, p.error_flag))
         live = false;
-      if (!live) flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+      if (!live) {  // abandoned: wait (bounded) for every tensor-core operation issued
+        umma_commit(bars.drain);
+        mbar_wait(bars.drain, 0);
+      }
     }
     __syncwarp();
   } else if (warp < NAW) {
@@ -1031,6 +1061,7 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
   p.groups = pl.groups;
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * kLog2e;
+  p.wait_ns = wait_report_ns();
   dim3 grid(pl.splits, kv->num_kv_heads, batch);
   const cudaError_t e = kv->head_dim == 128 ? launch_verify<128>(pl, tk, tv, p, grid, stream)
                                              : launch_verify<64>(pl, tk, tv, p, grid, stream);
@@ -1152,6 +1183,7 @@ extern "C" vg_status vg_sparse_verify_attention(
   p.u_max = sl.u_max;
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * kLog2e;
+  p.wait_ns = wait_report_ns();
   // the union pass, then the verify grid and its split merge (PDL chain)
   const size_t usmem = (size_t)kv->max_pages_per_seq * 4;
   static bool attr_done[64] = {false};

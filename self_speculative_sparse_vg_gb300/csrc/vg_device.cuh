@@ -12,7 +12,10 @@
 namespace vg {
 
 // A pipeline wait gives up after this many nanoseconds of %globaltimer and
-// reports VG_DEVERR_TIMEOUT instead of spinning forever.
+// reports VG_DEVERR_TIMEOUT instead of spinning forever.  A shorter bound
+// set with vg_set_wait_limit_ns only reports earlier: the wait then goes on
+// up to this bound, so that no copy or tensor-core operation it waits for is
+// abandoned while in flight.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -89,6 +92,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Wait for the phase with the given parity.  Past report_ns the wait ORs
+// VG_DEVERR_TIMEOUT into *flag and keeps waiting; it returns false (also
+// flagged) only when kWaitLimitNs has passed as well.  Under a bound shorter
+// than the default it polls with the non-blocking test and reads the timer
+// after every poll (a try_wait may itself sleep past a short bound).
+__device__ __forceinline__ bool mbar_wait_checked(uint64_t* bar, uint32_t parity,
+                                                  uint64_t report_ns, int32_t* flag) {
+  const bool short_bound = report_ns < kWaitLimitNs;
+  if (short_bound ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  const int polls = short_bound ? 1 : 32;
+  bool reported = false;
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < polls; ++i)
+      if (short_bound ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    const uint64_t dt = global_timer_ns() - t0;
+    if (!reported && (dt > report_ns || dt > kWaitLimitNs)) {
+      flag_error(flag, VG_DEVERR_TIMEOUT);
+      reported = true;
+    }
+    if (dt > kWaitLimitNs) return false;
   }
 }
 

@@ -1,11 +1,19 @@
 // Host-side helpers: status strings, device properties, TMA descriptors.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "vg_host.h"
 
 namespace vg {
+
+namespace {
+constexpr uint64_t kDefaultWaitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+std::atomic<uint64_t> g_wait_report_ns{kDefaultWaitNs};
+}  // namespace
+
+uint64_t wait_report_ns() { return g_wait_report_ns.load(std::memory_order_relaxed); }
 
 int device_sm_count() {
   static int cached[64] = {0};
@@ -145,4 +153,10 @@ extern "C" const char* vg_status_string(vg_status s) {
   return "VG_ERR_UNKNOWN";
 }
 
-extern "C" const char* vg_version(void) { return "0.1.0"; }
+extern "C" const char* vg_version(void) { return "0.2.0"; }
+
+extern "C" vg_status vg_set_wait_limit_ns(uint64_t limit_ns) {
+  vg::g_wait_report_ns.store(limit_ns == 0 ? vg::kDefaultWaitNs : limit_ns,
+                             std::memory_order_relaxed);
+  return VG_OK;
+}

@@ -18,6 +18,10 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Multiprocessor count of the current device (cached per device).
 int device_sm_count();
 
+// Bound after which a pipeline wait reports VG_DEVERR_TIMEOUT (set with
+// vg_set_wait_limit_ns; 1 s by default).  Kernels take it as a parameter.
+uint64_t wait_report_ns();
+
 // 4-D tiled TMA descriptor over a page pool viewed as
 // [num_pages][num_kv_heads][16][head_dim] bf16, box = 64 x 16 x 1 x 1 with the
 // 128-byte swizzle.  Cached per (pointer, shape).  Returns false on failure.

@@ -34,6 +34,7 @@ EXPORTED = (
     "vg_status_string", "vg_version",
     "vg_verify_noalloc_scratch_bytes", "vg_verify_attention_noalloc",
     "vg_sparse_verify_workspace_bytes", "vg_sparse_verify_attention",
+    "vg_set_wait_limit_ns",
 )
 
 
@@ -75,6 +76,7 @@ def _load():
         "vg_sparse_verify_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32, i32]),
         "vg_sparse_verify_attention": (i32, [kvp, vp, vp, i32, i32, i32, i32, f32, vp, vp, i32, vp,
                                              i32, vp, sz, vp, vp]),
+        "vg_set_wait_limit_ns": (i32, [ctypes.c_uint64]),
         "vg_status_string": (ctypes.c_char_p, [i32]),
         "vg_version": (ctypes.c_char_p, []),
     }
@@ -86,6 +88,12 @@ def _load():
 
 
 _lib = _load()
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    """vg_set_wait_limit_ns: waits longer than limit_ns report
+    DEVERR_TIMEOUT (and go on, up to 1 s); 0 restores the default."""
+    _check("vg_set_wait_limit_ns", _lib.vg_set_wait_limit_ns(int(limit_ns)))
 
 
 def status_string(s: int) -> str:
