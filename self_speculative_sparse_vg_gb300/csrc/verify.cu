@@ -61,6 +61,7 @@ struct VerifyParams {
   uint32_t* u_masks;   // [B][u_max] bit i: verify row i selected the page
   int32_t* u_count;    // [B]
   int u_max;
+  int persistent;      // dense: CTAs walk a list of units (gridDim.x CTAs in all)
   uint64_t wait_ns;    // a wait longer than this reports VG_DEVERR_TIMEOUT (and goes on)
   float scale, scale_log2;
 };
@@ -105,6 +106,9 @@ constexpr int kMPad = 128;             // UMMA M
 // 64 columns), O (<= 128 fp32), Q as the A operand (<= 64 bf16-pair columns).
 constexpr int kTmemCols = 512;
 constexpr int kSCol = 0, kOCol = 2 * kVTile, kQCol = kOCol + 128;
+// Q is double-buffered (a persistent CTA writes the next unit's Q while the
+// current unit's last scores are still being read): buffer i at kQCol + i *
+// HD / 2 (bf16 pairs), which ends at column 512 for head_dim 128.
 // O and l follow a new row maximum only past a 2^32 growth: until then P is
 // taken relative to the older reference, so one entry of P is at most 2^32
 // (exact range in bf16 and fp32, same relative precision) and l, O stay far
@@ -112,6 +116,7 @@ constexpr int kSCol = 0, kOCol = 2 * kVTile, kQCol = kOCol + 128;
 // wait for the last P.V, so it is kept off the common path.
 constexpr float kRescaleLog2 = 32.f;
 constexpr int kChunk = 32;             // columns a softmax pass holds in registers
+constexpr int kMaxPersistBatch = 64;   // sequences a persistent CTA's unit table holds
 constexpr int kCapStride = kChunk + 1; // floats per staged capture row
 
 template <int HD>
@@ -121,27 +126,74 @@ struct VerifyLayout {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kCapFloats = 4 * 16 * kCapStride;  // per-warp Collect-2 staging
   static constexpr int kAllFloats = 2 * 4 * kVTile;       // Collect-All partials [slot][warp]
-  static constexpr int kBars = 13;                        // besides the ring's 4 per stage
+  static constexpr int kBars = 15;                        // besides the ring's 4 per stage
   static constexpr int kSliceMax = 1024;                  // sparse: union pages of one split
+  static constexpr int kUnitTab = 4 * kMaxPersistBatch + 2; // persistent: per-sequence unit table
   static size_t bytes(int stages) {
     return 1024 + (size_t)stages * kStageBytes + (size_t)(kCapFloats + kAllFloats) * 4 +
-           (size_t)kSliceMax * 8 + (4 * (size_t)stages + kBars) * 8 + 16;
+           (size_t)kSliceMax * 8 + (4 * (size_t)stages + kBars) * 8 + 16 + kUnitTab * 4;
   }
 };
 
 struct VerifyBars {
-  uint64_t *kfull, *vfull, *kempty, *empty, *s_full, *p_full, *capfull, *capfree, *drain;
+  uint64_t *kfull, *vfull, *kempty, *empty, *s_full, *p_full, *capfull, *capfree, *drain, *qfull;
   int stages;
 };
 
-// Softmax warp of a copy; COLS = 128 / CS columns of each tile, handled in
-// chunks of 32 (two passes over TMEM when COLS > 32: maximum, then P).
+// Q rows of a unit -> tensor-memory buffer `buf` (the A operand), by one
+// softmax warp for its 32 lanes: lane c * RPC + m holds packed row m of copy
+// c, every other lane zero (its logits are exactly zero).
+template <int HD>
+__device__ __forceinline__ void write_q(const VerifyParams& p, uint32_t tmem, int buf, int b,
+                                        int h, int warp, int lane) {
+  const int M = p.m_rows;
+  const int CS = M <= 32 ? 4 : (M <= 64 ? 2 : 1);
+  const int RPC = kMPad / CS;
+  const int row = 32 * warp + lane;
+  const int cp = row / RPC, mm = row - cp * RPC;
+  const uint4* src = nullptr;
+  if (b >= 0 && cp < CS && mm < M) {
+    int i, qi;
+    row_of(mm, p.group, p.n_rows, i, qi);
+    src = reinterpret_cast<const uint4*>(
+        p.q + ((size_t)(b * p.n_rows + i) * p.num_q_heads + h * p.group + qi) * HD);
+  }
+  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16) + kQCol + buf * (HD / 2);
+#pragma unroll
+  for (int half = 0; half < HD / 64; ++half) {
+    uint4 x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = src ? src[half * 8 + k] : make_uint4(0, 0, 0, 0);
+    uint32_t v[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[4 * k] = x[k].x;
+      v[4 * k + 1] = x[k].y;
+      v[4 * k + 2] = x[k].z;
+      v[4 * k + 3] = x[k].w;
+    }
+    tmem_st32u(trow + half * 32, v);
+  }
+  tmem_st_wait();
+  tc_fence_before();
+}
+
+// Softmax warp of a copy for one unit of work (a split of one KV head of one
+// sequence); COLS = 128 / CS columns of each tile, handled in chunks of 32
+// (two passes over TMEM when COLS > 32: maximum, then P).  `tbase` is the
+// CTA's count of tiles before this unit: ring stages, S/P buffers and their
+// barrier phases follow that running count across units.  When the CTA has a
+// next unit (nb >= 0), its Q goes to tensor-memory buffer qbuf_next (arrival
+// on qfull[qbuf_next]) before this unit's epilogue, so that the tensor cores
+// can start its scores meanwhile.  `scratch` (the capture staging area, idle
+// by then) holds the copies' merge.
 template <int HD, int COLS, int CM, bool SP>
 __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const VerifyBars& bars,
-                                               uint8_t* ring, float* cap_s, float* all_s,
+                                               float* scratch, float* cap_s, float* all_s,
                                                const int32_t* sl_page, const uint32_t* sl_mask,
                                                int sl_n, uint32_t tmem, int b, int h, int split,
-                                               int t0, int ntiles, int L, int warp, int lane) {
+                                               int t0, int ntiles, int L, int tbase, int& hs,
+                                               int nb, int nh, int qbuf_next, int warp, int lane) {
   constexpr int CS = kVTile / COLS;       // copies
   constexpr int QC = 4 / CS;              // warps (TMEM quadrants) per copy
   constexpr int RPC = 32 * QC;            // rows per copy
@@ -170,7 +222,8 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
   bool live = true;
 
   for (int lt = 0; lt < ntiles; ++lt) {
-    const int sb = lt & 1, u = lt >> 1;
+    const int T = tbase + lt;  // the CTA's running tile index
+    const int sb = T & 1, u = T >> 1;
     const int tile_pos = (t0 + lt) * kVTile;
     const uint32_t sbuf = trow + kSCol + sb * kVTile;
     if (live && !mbar_wait_checked(&bars.s_full[sb], u & 1, p.wait_ns, p.error_flag)) live = false;
@@ -274,12 +327,14 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
     }
     if (cap_all && cpos < L) {
       // across the copy's warps, in order, through shared memory
-      const int slot = lt & 1;
+      // hs counts this copy's handshakes in the CTA (tiles past the prefix
+      // have none), so that the barrier phases hold across units
+      const int slot = hs & 1;
       const int cb = c * 2 + slot;  // this copy's handshake barrier of the slot
       float* part = all_s + slot * 4 * kVTile;
       if (wq != 0) {
-        if (lt >= 2 && live &&
-            !mbar_wait_checked(&bars.capfree[cb], ((lt >> 1) - 1) & 1, p.wait_ns, p.error_flag))
+        if (hs >= 2 && live &&
+            !mbar_wait_checked(&bars.capfree[cb], ((hs >> 1) - 1) & 1, p.wait_ns, p.error_flag))
           live = false;
 #pragma unroll
         for (int k = 0; k < NCH; ++k) part[warp * kVTile + k * kChunk + lane] = call[k];
@@ -287,7 +342,7 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
         if (lane == 0) mbar_arrive(&bars.capfull[cb]);
       } else {
         if (nwc > 1 && live &&
-            !mbar_wait_checked(&bars.capfull[cb], (lt >> 1) & 1, p.wait_ns, p.error_flag))
+            !mbar_wait_checked(&bars.capfull[cb], (hs >> 1) & 1, p.wait_ns, p.error_flag))
           live = false;
         float* dst = p.capture + ((size_t)b * p.num_kv_heads + h) * p.max_prefix + cpos;
 #pragma unroll
@@ -299,6 +354,7 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
         __syncwarp();
         if (nwc > 1 && lane == 0) mbar_arrive(&bars.capfree[cb]);
       }
+      ++hs;
     }
 
     // -------- online softmax (base 2) with a lazily moved reference
@@ -309,9 +365,9 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
       const float corr = (mn == -INFINITY) ? 1.f : ex2(m_used - mn);
       lsum *= corr;
       if (lt > 0) {  // O holds P(0..t-1) V: wait for the last P.V, then scale the row
-        const int pst = (lt - 1) % stages;
+        const int pst = (T - 1) % stages;
         if (live &&
-            !mbar_wait_checked(&bars.empty[pst], ((lt - 1) / stages) & 1, p.wait_ns, p.error_flag))
+            !mbar_wait_checked(&bars.empty[pst], ((T - 1) / stages) & 1, p.wait_ns, p.error_flag))
           live = false;
         tc_fence_after();
 #pragma unroll 1
@@ -362,35 +418,30 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars.p_full[sb]);
   }
+  // -------- the next unit's Q, so that its scores can start during this
+  // unit's epilogue (the buffer's previous unit has had all its scores read)
+  if (nb >= 0) {
+    write_q<HD>(p, tmem, qbuf_next, nb, nh, warp, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars.qfull[qbuf_next]);
+  }
+
   // -------- epilogue: merge the copies, then this lane's row of O
   if (ntiles > 0)
-    mbar_wait_checked(&bars.empty[(ntiles - 1) % stages], ((ntiles - 1) / stages) & 1, p.wait_ns,
-                      p.error_flag);
+    mbar_wait_checked(&bars.empty[(tbase + ntiles - 1) % stages],
+                      ((tbase + ntiles - 1) / stages) & 1, p.wait_ns, p.error_flag);
   tc_fence_after();
-  // scratch in the idle ring, column-major so that a warp's 32 rows are 32
-  // consecutive floats: so[copy - 1][d][row], sml[copy - 1][{m, l}][row]
-  float* so = reinterpret_cast<float*>(ring);
-  float* sml = so + (CS - 1) * RPC * HD;
+  // scratch, column-major so that a warp's 32 rows are 32 consecutive
+  // floats: sml[copy - 1][{m, l}][row], then one 32-column chunk of O per
+  // copy so[copy - 1][d][row]
+  float* sml = scratch;
+  float* so = scratch + (CS > 1 ? (CS - 1) * 2 * RPC : 0);
   if (CS > 1 && c > 0) {
-#pragma unroll 1
-    for (int cc = 0; cc < HD / 32; ++cc) {
-      float o[32];
-      if (ntiles > 0) {
-        tmem_ld32(trow + kOCol + cc * 32, o);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) o[k] = 0.f;
-      }
-      float* d = so + ((size_t)(c - 1) * HD + cc * 32) * RPC + m;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) d[k * RPC] = o[k];
-    }
     sml[((c - 1) * 2) * RPC + m] = m_used;
     sml[((c - 1) * 2 + 1) * RPC + m] = lsum;
   }
   if (CS > 1) named_barrier_sync(1, 4 * 32);  // all four softmax warps
-  if (c > 0) return;
-  // weights of the copies relative to the largest reference
+  // weights of the copies relative to the largest reference (copy 0's warps)
   float mxr = m_used;
   for (int c2 = 1; c2 < CS; ++c2) mxr = fmaxf(mxr, sml[((c2 - 1) * 2) * RPC + m]);
   const float ref = safe_ref(mxr);
@@ -415,12 +466,20 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
 #pragma unroll
       for (int k = 0; k < 32; ++k) o[k] = 0.f;
     }
-    if (m < M) {
+    if (CS > 1) {  // copies 1.. hand their chunk to copy 0
+      if (c > 0) {
+        float* d = so + (size_t)(c - 1) * 32 * RPC + m;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) d[k * RPC] = o[k];
+      }
+      named_barrier_sync(1, 4 * 32);
+    }
+    if (c == 0 && m < M) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) o[k] *= w0;
 #pragma unroll
       for (int c2 = 1; c2 < CS; ++c2) {
-        const float* src = so + ((size_t)(c2 - 1) * HD + cc * 32) * RPC + m;
+        const float* src = so + (size_t)(c2 - 1) * 32 * RPC + m;
 #pragma unroll
         for (int k = 0; k < 32; ++k) o[k] += wc[c2 - 1] * src[k * RPC];
       }
@@ -443,7 +502,9 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
           *reinterpret_cast<float4*>(dst + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
       }
     }
+    if (CS > 1) named_barrier_sync(1, 4 * 32);  // the chunk is read before the next is written
   }
+  if (c > 0) return;
   if (m < M && p.splits > 1) {
     float* ml = p.part_ml + ((bh * p.splits + split) * M + m) * 2;
     ml[0] = mxr;
@@ -466,12 +527,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = p.group, R = p.n_rows, M = p.m_rows;
+  const int R = p.n_rows, M = p.m_rows;
   const int NS = (M + 31) >> 5;
   const int CS = M <= 32 ? 4 : (M <= 64 ? 2 : 1);  // row copies
-  const int RPC = kMPad / CS;                        // TMEM lanes per copy
   const int NAW = CS == 1 ? NS : 4;                  // softmax warps at work
   const int stages = p.stages;
 
@@ -491,7 +550,9 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   bars.capfull = bars.p_full + 2;     // [copy][slot]: Collect-All partials written
   bars.capfree = bars.capfull + 4;    // [copy][slot]: Collect-All slot read
   bars.drain = bars.capfree + 4;      // every tensor-core operation issued so far done
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars.drain + 1);
+  bars.qfull = bars.drain + 1;        // [buffer]: a later unit's Q written (persistent CTAs)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars.qfull + 2);
+  int* utab = reinterpret_cast<int*>(tmem_holder + 4);  // persistent: per-sequence unit table
 
   // the K/V tensor maps are kernel parameters, independent of earlier
   // kernels: fetch their descriptors before anything else so that the first
@@ -503,58 +564,129 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   // programmatic dependent launch: inputs may come from the previous kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  // The producer reads the page ids of its first 4 tiles while the length is
-  // still in flight (within the page-table row; ids past the sequence are
-  // dropped once the length is known).
   constexpr int kPagesPerTile = kVTile / kPageSize;  // 8
-  int pre_id = -1;
-  if (!SP && warp == kProducerWarp) {
-    const int lp = split * p.tiles_per_split * kPagesPerTile + lane;
-    if (lp < p.max_pages_per_seq) pre_id = p.page_table[(size_t)b * p.max_pages_per_seq + lp];
+
+  // ---- the CTA's units of work.  One CTA per (split, KV head, sequence)
+  // runs one unit.  A persistent CTA (dense only) takes every gridDim.x-th
+  // unit of a list built from the device lengths: the full splits of every
+  // (sequence, KV head) first, then the shorter last splits, so that the
+  // round-robin keeps the CTAs balanced.
+  const bool persistent = !SP && p.persistent;
+  int n_units = 1;
+  int pre_id = -1;  // page id of lane's page in the first unit's first window (one CTA per unit)
+  if (persistent) {
+    // utab: [0, B] prefix of full units, [B+1, 2B+1] prefix of last
+    // (partial) units, [2B+2, 3B+1] tiles per sequence, [3B+2, 4B+1] lengths
+    const int B = p.batch;
+    if (threadIdx.x < B) {
+      const int bb = threadIdx.x;
+      const int L = p.prefix_lens[bb];
+      const bool ok = L >= 1 && L <= p.max_prefix &&
+                      (L + R + kPageSize - 1) / kPageSize <= p.max_pages_per_seq;
+      if (!ok && blockIdx.x == 0) flag_error(p.error_flag, VG_DEVERR_LENGTH);
+      const int tiles = ok ? (L + R + kVTile - 1) / kVTile : 0;
+      utab[2 * B + 2 + bb] = tiles;
+      utab[3 * B + 2 + bb] = L;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int f = 0, q = 0;
+      for (int bb = 0; bb < B; ++bb) {
+        utab[bb] = f;
+        utab[B + 1 + bb] = q;
+        const int tiles = utab[2 * B + 2 + bb];
+        f += p.num_kv_heads * (tiles / p.tiles_per_split);
+        q += p.num_kv_heads * (tiles % p.tiles_per_split != 0 ? 1 : 0);
+      }
+      utab[B] = f;
+      utab[2 * B + 1] = q;
+    }
+    __syncthreads();
+    const int total = utab[B] + utab[2 * B + 1];
+    n_units = blockIdx.x < total ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  } else if (!SP && warp == kProducerWarp) {
+    // the page ids of the first 4 tiles are read while the length is still
+    // in flight (within the page-table row; ids past the sequence are dropped
+    // once the length is known)
+    const int lp = blockIdx.x * p.tiles_per_split * kPagesPerTile + lane;
+    if (lp < p.max_pages_per_seq)
+      pre_id = p.page_table[(size_t)blockIdx.z * p.max_pages_per_seq + lp];
   }
-  const int L = p.prefix_lens[b];
-  const int n_b = L + R;
-  if (L < 1 || L > p.max_prefix || (n_b + kPageSize - 1) / kPageSize > p.max_pages_per_seq) {
-    if (threadIdx.x == 0 && split == 0 && h == 0) flag_error(p.error_flag, VG_DEVERR_LENGTH);
+  // unit k of this CTA: (sequence, KV head, split), its first tile and tile
+  // count, the sequence's length (a negative b: no such unit, or a skipped
+  // sequence)
+  auto unit_of = [&](int k, int& b, int& h, int& split, int& t0, int& ntiles, int& L) {
+    b = -1;
+    h = split = t0 = ntiles = L = 0;
+    if (k >= n_units) return;
+    if (!persistent) {
+      b = blockIdx.z;
+      h = blockIdx.y;
+      split = blockIdx.x;
+      L = p.prefix_lens[b];
+      const int n_b = L + R;
+      if (L < 1 || L > p.max_prefix || (n_b + kPageSize - 1) / kPageSize > p.max_pages_per_seq) {
+        b = -1;
+        return;
+      }
+      const int u_n = SP ? min(p.u_count[b], p.u_max) : 0;  // union pages of this sequence
+      const int tiles_b = SP ? (u_n + kPagesPerTile - 1) / kPagesPerTile : (n_b + kVTile - 1) / kVTile;
+      // Dense: split s streams tiles [s tps, (s + 1) tps).  Sparse: the
+      // union's size is known only on the device, so split s takes tiles s,
+      // s + S, ... and every split has work whatever the union's size.
+      t0 = SP ? 0 : split * p.tiles_per_split;
+      ntiles = SP ? (split < tiles_b ? min((tiles_b - split + p.splits - 1) / p.splits,
+                                          p.tiles_per_split)
+                                     : 0)
+                  : max(0, min(t0 + p.tiles_per_split, tiles_b) - t0);
+      return;
+    }
+    const int B = p.batch, tps = p.tiles_per_split;
+    int i = blockIdx.x + k * gridDim.x;
+    const bool full = i < utab[B];
+    if (!full) i -= utab[B];
+    const int* pre = full ? utab : utab + B + 1;
+    int bb = 0;
+    while (bb + 1 < B && pre[bb + 1] <= i) ++bb;
+    const int j = i - pre[bb];
+    const int tiles = utab[2 * B + 2 + bb];
+    b = bb;
+    L = utab[3 * B + 2 + bb];
+    if (full) {
+      const int nf = tiles / tps;
+      h = j / nf;
+      split = j - h * nf;
+    } else {
+      h = j;
+      split = tiles / tps;
+    }
+    t0 = split * tps;
+    ntiles = min(tps, tiles - t0);
+  };
+
+  int b0, h0, split0, t00, nt0, L0;
+  unit_of(0, b0, h0, split0, t00, nt0, L0);
+  if (persistent && warp == kProducerWarp && b0 >= 0) {
+    const int lp = t00 * kPagesPerTile + lane;
+    if (lp < (L0 + R + kPageSize - 1) / kPageSize)
+      pre_id = p.page_table[(size_t)b0 * p.max_pages_per_seq + lp];
+  }
+  if (!persistent && b0 < 0) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      flag_error(p.error_flag, VG_DEVERR_LENGTH);
     return;  // uniform for every CTA of this sequence
   }
-  const int npages_b = (n_b + kPageSize - 1) / kPageSize;
-  constexpr int kPagesPerTileC = kVTile / kPageSize;
-  const int u_n = SP ? min(p.u_count[b], p.u_max) : 0;  // union pages of this sequence
-  const int tiles_b = SP ? (u_n + kPagesPerTileC - 1) / kPagesPerTileC : (n_b + kVTile - 1) / kVTile;
-  // Dense: split s streams tiles [s tps, (s + 1) tps).  Sparse: the union's
-  // size is known only on the device, so split s takes tiles s, s + S, ...
-  // and every split has work whatever the union's size.
-  const int t0 = SP ? 0 : split * p.tiles_per_split;
-  const int ntiles =
-      SP ? (split < tiles_b ? min((tiles_b - split + p.splits - 1) / p.splits, p.tiles_per_split) : 0)
-         : max(0, min(t0 + p.tiles_per_split, tiles_b) - t0);
+  if (n_units == 0) return;  // a persistent CTA without work (uniform)
   int sl_n = 0;  // slots of this split's union slice (sparse; -1 past the union)
   if constexpr (SP) {
-    sl_n = min(ntiles * kPagesPerTileC, Lay::kSliceMax);
+    const int u_n = min(p.u_count[b0], p.u_max);
+    sl_n = min(nt0 * kPagesPerTile, Lay::kSliceMax);
     for (int i = threadIdx.x; i < sl_n; i += kVerifyThreads) {
-      const int lt = i / kPagesPerTileC;
-      const int e = (split + lt * p.splits) * kPagesPerTileC + (i - lt * kPagesPerTileC);
-      sl_page[i] = e < u_n ? p.u_pages[(size_t)b * p.u_max + e] : -1;
-      sl_mask[i] = e < u_n ? p.u_masks[(size_t)b * p.u_max + e] : 0u;
+      const int lt = i / kPagesPerTile;
+      const int e = (split0 + lt * p.splits) * kPagesPerTile + (i - lt * kPagesPerTile);
+      sl_page[i] = e < u_n ? p.u_pages[(size_t)b0 * p.u_max + e] : -1;
+      sl_mask[i] = e < u_n ? p.u_masks[(size_t)b0 * p.u_max + e] : 0u;
     }
-  }
-
-  // Q rows of the softmax warps: loads issued now, written to tensor memory
-  // once it is allocated (lane c * RPC + m holds packed row m of copy c,
-  // every other lane zero: its logits are exactly zero)
-  uint4 qreg[HD / 8];
-  if (warp < 4) {
-    const int row = 32 * warp + lane;
-    const int cp = row / RPC, mm = row - cp * RPC;
-    const uint4* src = nullptr;
-    if (cp < CS && mm < M) {
-      int i, qi;
-      row_of(mm, g, R, i, qi);
-      src = reinterpret_cast<const uint4*>(p.q + ((size_t)(b * R + i) * p.num_q_heads + h * g + qi) * HD);
-    }
-#pragma unroll
-    for (int k = 0; k < HD / 8; ++k) qreg[k] = src ? src[k] : make_uint4(0, 0, 0, 0);
   }
 
   if (threadIdx.x == 0) {
@@ -568,6 +700,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.s_full[s], 1);
       mbar_init(&bars.p_full[s], NAW);
+      mbar_init(&bars.qfull[s], NAW);
     }
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars.capfull[s], nwc > 1 ? nwc - 1 : 1);
@@ -581,27 +714,13 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // Q is handed from the softmax warps to the MMA warp through named barrier
-  // 2 (warps 0-3 and 5); the producer starts its loads at once
+  // The first unit's Q (buffer 0) and zero rows in buffer 1 (rows that no
+  // unit fills) are handed from the softmax warps to the MMA warp through
+  // named barrier 2 (warps 0-3 and 5); later units' Q through qfull.
   constexpr int kQReadyBar = 2, kQReadyThreads = 5 * 32;
   if (warp < 4) {
-    // Q -> tensor memory (A operand)
-    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
-#pragma unroll
-    for (int half = 0; half < HD / 64; ++half) {
-      uint32_t v[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 x = qreg[half * 8 + k];
-        v[4 * k] = x.x;
-        v[4 * k + 1] = x.y;
-        v[4 * k + 2] = x.z;
-        v[4 * k + 3] = x.w;
-      }
-      tmem_st32u(trow + kQCol + half * 32, v);
-    }
-    tmem_st_wait();
-    tc_fence_before();
+    write_q<HD>(p, tmem, 0, b0, h0, warp, lane);
+    if (n_units > 1) write_q<HD>(p, tmem, 1, -1, 0, warp, lane);
     named_barrier_sync(kQReadyBar, kQReadyThreads);
   } else if (warp == kMmaWarp) {
     named_barrier_sync(kQReadyBar, kQReadyThreads);
@@ -616,14 +735,28 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
     // waits for are not held back by the softmax of older tiles.  The warp
     // fetches the page ids of 4 tiles (32 ids, one per lane) in one round
     // trip; each lane issues one TMA box (16 positions x 64 dims) of a half.
-    if (ntiles > 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      constexpr int kHalfBoxes = kPagesPerTile * (HD / 64);  // boxes of one of K / V
-      const int pi = lane / (HD / 64), dh = lane % (HD / 64);
+    // Across a persistent CTA's units the ring keeps streaming: the next
+    // unit's first page ids are read while the current unit is loaded.
+    const uint64_t pol = l2_policy_evict_first();
+    constexpr int kHalfBoxes = kPagesPerTile * (HD / 64);  // boxes of one of K / V
+    const int pi = lane / (HD / 64), dh = lane % (HD / 64);
+    int k_armed = 0, v_armed = 0;  // K / V tile loads issued (the CTA's running count)
+    bool aborted = false;
+    int b = b0, h = h0, split = split0, t0 = t00, ntiles = nt0, L = L0;
+    for (int k = 0; k < n_units && !aborted; ++k) {
+      int nb, nh, nsplit, nt0n, nntiles, nL;
+      unit_of(k + 1, nb, nh, nsplit, nt0n, nntiles, nL);
+      int pre_next = -1;  // the next unit's first page ids, read ahead
+      if (nb >= 0) {
+        const int lp = nt0n * kPagesPerTile + lane;
+        const int npg = (nL + R + kPageSize - 1) / kPageSize;
+        if (lp < npg) pre_next = p.page_table[(size_t)nb * p.max_pages_per_seq + lp];
+      }
+      const int npages_b = (L + R + kPageSize - 1) / kPageSize;
+      const int tbase = k_armed;
       // page ids of tiles [4w, 4w + 4) for the window w of the K tile, and of
       // the window before it (V runs one tile behind)
       int id_cur = p.num_pages, id_prev = p.num_pages;
-      int k_armed = 0, v_armed = 0;  // K / V tile loads issued
       for (int kt = 0; kt <= ntiles; ++kt) {
         const int vt = kt - 1;
         const bool new_window = kt < ntiles && (kt & 3) == 0;
@@ -644,13 +777,17 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
           }
         }
         if (kt < ntiles) {
-          const int st = kt % stages;
+          const int T = tbase + kt;
+          const int st = T % stages;
           int go = 1;
-          if (lane == 0 && kt >= stages)
-            go = mbar_wait_checked(&bars.kempty[st], ((kt / stages) - 1) & 1, p.wait_ns,
+          if (lane == 0 && T >= stages)
+            go = mbar_wait_checked(&bars.kempty[st], ((T / stages) - 1) & 1, p.wait_ns,
                                    p.error_flag);
           go = __shfl_sync(0xffffffffu, go, 0);
-          if (!go) break;  // the consumer is gone: stop, then drain what is in flight
+          if (!go) {  // the consumer is gone: stop, then drain what is in flight
+            aborted = true;
+            break;
+          }
           const int id = __shfl_sync(0xffffffffu, id_cur, (kt & 3) * 8 + (pi & 7));
           if (lane == 0) mbar_arrive_expect_tx(&bars.kfull[st], kTileBytes);
           __syncwarp();
@@ -661,13 +798,17 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
           ++k_armed;
         }
         if (vt >= 0) {
-          const int st = vt % stages;
+          const int T = tbase + vt;
+          const int st = T % stages;
           int go = 1;
-          if (lane == 0 && vt >= stages)
-            go = mbar_wait_checked(&bars.empty[st], ((vt / stages) - 1) & 1, p.wait_ns,
+          if (lane == 0 && T >= stages)
+            go = mbar_wait_checked(&bars.empty[st], ((T / stages) - 1) & 1, p.wait_ns,
                                    p.error_flag);
           go = __shfl_sync(0xffffffffu, go, 0);
-          if (!go) break;
+          if (!go) {
+            aborted = true;
+            break;
+          }
           const int idv = new_window ? id_prev : id_cur;  // V's tile is in the window before
           const int id = __shfl_sync(0xffffffffu, idv, (vt & 3) * 8 + (pi & 7));
           if (lane == 0) mbar_arrive_expect_tx(&bars.vfull[st], kTileBytes);
@@ -680,85 +821,108 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
           ++v_armed;
         }
       }
-      // After a normal run every load has been consumed.  After an abandoned
-      // run, wait (bounded) for the last load armed on every stage, so that no
-      // copy is still writing into shared memory when the CTA leaves.
-      if (lane == 0 && (k_armed < ntiles || v_armed < ntiles)) {
-        for (int s = 0; s < stages; ++s) {
-          if (k_armed > s)
-            mbar_wait(&bars.kfull[s], (((k_armed - 1 - s) / stages)) & 1);
-          if (v_armed > s)
-            mbar_wait(&bars.vfull[s], (((v_armed - 1 - s) / stages)) & 1);
-        }
-      }
-      __syncwarp();
+      b = nb;
+      h = nh;
+      split = nsplit;
+      t0 = nt0n;
+      ntiles = nntiles;
+      L = nL;
+      pre_id = pre_next;
     }
+    // After a normal run every load has been consumed.  After an abandoned
+    // run, wait (bounded) for the last load armed on every stage, so that no
+    // copy is still writing into shared memory when the CTA leaves.
+    if (lane == 0 && aborted) {
+      for (int s = 0; s < stages; ++s) {
+        if (k_armed > s) mbar_wait(&bars.kfull[s], (((k_armed - 1 - s) / stages)) & 1);
+        if (v_armed > s) mbar_wait(&bars.vfull[s], (((v_armed - 1 - s) / stages)) & 1);
+      }
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issue
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0) {
       const uint32_t ring_u = smem_u32(ring);
       constexpr uint32_t id_qk = umma_idesc_bf16(kMPad, kVTile, 0, 0);
       constexpr uint32_t id_pv = umma_idesc_bf16(kMPad, HD, 0, 1);
-      // Issue whichever is ready: S(t) = Q K(t)^T (needs tile t and P(t - 2) V
-      // done, which frees its S buffer) or O += P(t) V(t) (needs P(t)).
-      int nq = 0, np = 0;
       bool live = true, reported = false;
+      int tbase = 0;
       uint64_t last = global_timer_ns();
-      while (np < ntiles) {
-        bool moved = false;
-        if (nq < ntiles) {
-          const int st = nq % stages, sb = nq & 1;
-          if (mbar_test_wait(&bars.kfull[st], (nq / stages) & 1) &&
-              (nq < 2 || mbar_test_wait(&bars.empty[(nq - 2) % stages], ((nq - 2) / stages) & 1))) {
+      for (int k = 0; k < n_units && live; ++k) {
+        int b, h, split, t0, ntiles, L;
+        unit_of(k, b, h, split, t0, ntiles, L);
+        const int qbuf = k & 1;
+        // a later unit's Q is written by the softmax warps (qfull), the first
+        // one was handed over before the roles split
+        bool q_ready = k == 0;
+        // Issue whichever is ready: S(t) = Q K(t)^T (needs tile t and P(t - 2)
+        // V done, which frees its S buffer) or O += P(t) V(t) (needs P(t)).
+        int nq = 0, np = 0;
+        while (np < ntiles) {
+          bool moved = false;
+          if (!q_ready && mbar_test_wait(&bars.qfull[qbuf], ((k - 1) >> 1) & 1)) {
             tc_fence_after();
-            const uint32_t kb = ring_u + st * kStageBytes;
+            q_ready = true;
+          }
+          if (q_ready && nq < ntiles) {
+            const int T = tbase + nq;
+            const int st = T % stages, sb = T & 1;
+            if (mbar_test_wait(&bars.kfull[st], (T / stages) & 1) &&
+                (T < 2 || mbar_test_wait(&bars.empty[(T - 2) % stages], ((T - 2) / stages) & 1))) {
+              tc_fence_after();
+              const uint32_t kb = ring_u + st * kStageBytes;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-              const uint64_t bd =
-                  umma_smem_desc(kb + (ks >> 2) * Lay::kHalfBytes + (ks & 3) * 32, 16, 1024);
-              umma_bf16_ts(tmem + kSCol + sb * kVTile, tmem + kQCol + ks * 8, bd, id_qk, ks > 0);
+              for (int ks = 0; ks < KS; ++ks) {
+                const uint64_t bd =
+                    umma_smem_desc(kb + (ks >> 2) * Lay::kHalfBytes + (ks & 3) * 32, 16, 1024);
+                umma_bf16_ts(tmem + kSCol + sb * kVTile, tmem + kQCol + qbuf * (HD / 2) + ks * 8,
+                             bd, id_qk, ks > 0);
+              }
+              umma_commit(&bars.s_full[sb]);
+              umma_commit(&bars.kempty[st]);  // K half of the stage free for the producer
+              ++nq;
+              moved = true;
             }
-            umma_commit(&bars.s_full[sb]);
-            umma_commit(&bars.kempty[st]);  // K half of the stage free for the producer
-            ++nq;
-            moved = true;
           }
-        }
-        if (np < nq) {
-          const int st = np % stages, sb = np & 1;
-          if (mbar_test_wait(&bars.p_full[sb], (np >> 1) & 1) &&
-              mbar_test_wait(&bars.vfull[st], (np / stages) & 1)) {
-            tc_fence_after();
-            const uint32_t vb = ring_u + st * kStageBytes + kTileBytes;
+          if (np < nq) {
+            const int T = tbase + np;
+            const int st = T % stages, sb = T & 1;
+            if (mbar_test_wait(&bars.p_full[sb], (T >> 1) & 1) &&
+                mbar_test_wait(&bars.vfull[st], (T / stages) & 1)) {
+              tc_fence_after();
+              const uint32_t vb = ring_u + st * kStageBytes + kTileBytes;
 #pragma unroll
-            for (int ks = 0; ks < kVTile / 16; ++ks) {
-              // V is MN-major: 64-dim blocks one half-tile apart, 8-position groups 1 KB apart
-              const uint64_t bd = umma_smem_desc(vb + ks * 16 * 128, Lay::kHalfBytes, 1024);
-              umma_bf16_ts(tmem + kOCol, tmem + kSCol + sb * kVTile + ks * 8, bd, id_pv,
-                           (np > 0 || ks > 0));
+              for (int ks = 0; ks < kVTile / 16; ++ks) {
+                // V is MN-major: 64-dim blocks one half-tile apart, 8-position groups 1 KB apart
+                const uint64_t bd = umma_smem_desc(vb + ks * 16 * 128, Lay::kHalfBytes, 1024);
+                umma_bf16_ts(tmem + kOCol, tmem + kSCol + sb * kVTile + ks * 8, bd, id_pv,
+                             (np > 0 || ks > 0));
+              }
+              umma_commit(&bars.empty[st]);
+              ++np;
+              moved = true;
             }
-            umma_commit(&bars.empty[st]);
-            ++np;
-            moved = true;
+          }
+          if (moved) {
+            last = global_timer_ns();
+          } else {
+            const uint64_t idle = global_timer_ns() - last;
+            if (!reported && (idle > p.wait_ns || idle > kWaitLimitNs)) {
+              flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
+              reported = true;
+            }
+            if (idle > kWaitLimitNs) {
+              live = false;
+              break;
+            }
           }
         }
-        if (moved) {
-          last = global_timer_ns();
-        } else {
-          const uint64_t idle = global_timer_ns() - last;
-          if (!reported && (idle > p.wait_ns || idle > kWaitLimitNs)) {
-            flag_error(p.error_flag, VG_DEVERR_TIMEOUT);
-            reported = true;
-          }
-          if (idle > kWaitLimitNs) {
-            live = false;
-            break;
-          }
-        }
+        tbase += ntiles;
       }
       // the last P.V has finished before the tensor memory is released
-      if (live && !mbar_wait_checked(&bars.empty[(ntiles - 1) % stages],
-                                     ((ntiles - 1) / stages) & 1, p.wait_ns, p.error_flag))
+      if (live && tbase > 0 &&
+          !mbar_wait_checked(&bars.empty[(tbase - 1) % stages], ((tbase - 1) / stages) & 1,
+                             p.wait_ns, p.error_flag))
         live = false;
       if (!live) {  // abandoned: wait (bounded) for every tensor-core operation issued
         umma_commit(bars.drain);
@@ -768,12 +932,22 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
     __syncwarp();
   } else if (warp < NAW) {
     // ---------------------------------------------------------- softmax
-    if (CS == 4)
-      verify_softmax<HD, 32, CM, SP>(p, bars, ring, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, warp, lane);
-    else if (CS == 2)
-      verify_softmax<HD, 64, CM, SP>(p, bars, ring, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, warp, lane);
-    else
-      verify_softmax<HD, 128, CM, SP>(p, bars, ring, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, warp, lane);
+    float* scratch = cap_s;  // the capture staging and slice area, idle in an epilogue
+    int tbase = 0, hs = 0;
+    for (int k = 0; k < n_units; ++k) {
+      int b, h, split, t0, ntiles, L;
+      unit_of(k, b, h, split, t0, ntiles, L);
+      int nb, nh, nsplit, nt0n, nntiles, nL;
+      unit_of(k + 1, nb, nh, nsplit, nt0n, nntiles, nL);
+      const int qn = (k + 1) & 1;
+      if (CS == 4)
+        verify_softmax<HD, 32, CM, SP>(p, bars, scratch, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
+      else if (CS == 2)
+        verify_softmax<HD, 64, CM, SP>(p, bars, scratch, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
+      else
+        verify_softmax<HD, 128, CM, SP>(p, bars, scratch, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
+      tbase += ntiles;
+    }
   }
   tc_fence_before();
   __syncthreads();  // every TMEM access and every MMA of this CTA is done
@@ -799,11 +973,17 @@ __global__ void __launch_bounds__(kMergeThreads) verify_merge_kernel(const Verif
       (L + p.n_rows + kPageSize - 1) / kPageSize > p.max_pages_per_seq)
     return;  // the verify kernel skipped this sequence (and flagged it)
   const int M = p.m_rows, S = p.splits;
+  // splits with work: dense, split s streams tiles [s tps, (s + 1) tps) of
+  // the sequence's; sparse, split s takes union tiles s, s + S, ...
+  const int tiles_b = p.u_count ? (min(p.u_count[b], p.u_max) + kVTile / kPageSize - 1) / (kVTile / kPageSize)
+                                : (L + p.n_rows + kVTile - 1) / kVTile;
+  const int s_work = p.u_count ? min(S, tiles_b)
+                               : min(S, (tiles_b + p.tiles_per_split - 1) / p.tiles_per_split);
   const size_t bh = (size_t)b * p.num_kv_heads + h;
   int i, qi;
   row_of(m, p.group, p.n_rows, i, qi);
   merge_splits<HD>(p.part_o + (bh * S * M + m) * HD, (size_t)M * HD, p.part_ml + (bh * S * M + m) * 2,
-                   (size_t)M * 2, S,
+                   (size_t)M * 2, s_work,
                    p.out + ((size_t)(b * p.n_rows + i) * p.num_q_heads + h * p.group + qi) * HD, smem_f,
                    p.capture_mode == VG_CAPTURE_ALL_ROWS
                        ? p.capture + p.lse_offset +
@@ -889,12 +1069,13 @@ __global__ void __launch_bounds__(kUnionThreads)
 
 struct VerifyPlan {
   int hd, m_rows, m_tiles, groups, splits, tiles_per_split, stages;
+  int persistent, grid_x;  // dense: persistent CTAs walking the units, and their number
   size_t smem_bytes;
   size_t off_ml, ws_bytes;
 };
 
 bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, int head_dim,
-                      int max_prefix, int num_splits, VerifyPlan* pl) {
+                      int max_prefix, int num_splits, VerifyPlan* pl, bool sparse = false) {
   if (batch <= 0 || n_rows <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_prefix <= 0)
     return false;
   const int g = num_q_heads / num_kv_heads;
@@ -917,6 +1098,13 @@ bool make_verify_plan(int batch, int n_rows, int num_q_heads, int num_kv_heads, 
   if (ceil_div(tiles, tps) > kMaxSplits) tps = ceil_div(tiles, kMaxSplits);
   pl->tiles_per_split = tps;
   pl->splits = ceil_div(tiles, tps);
+  // More units than SMs (and a batch the unit table holds): persistent CTAs,
+  // one per SM, each walking its share of the units, so that one unit's
+  // prologue and epilogue overlap the streaming of the next.
+  const long long units = (long long)batch * num_kv_heads * pl->splits;
+  const int sms = device_sm_count();
+  pl->persistent = !sparse && batch <= kMaxPersistBatch && units > sms ? 1 : 0;
+  pl->grid_x = pl->persistent ? sms : pl->splits;
   auto smem_for = [&](int stages) {
     return head_dim == 128 ? VerifyLayout<128>::bytes(stages) : VerifyLayout<64>::bytes(stages);
   };
@@ -1062,7 +1250,8 @@ extern "C" vg_status vg_verify_attention(const vg_paged_kv* kv, const void* q,
   p.scale = softmax_scale;
   p.scale_log2 = softmax_scale * kLog2e;
   p.wait_ns = wait_report_ns();
-  dim3 grid(pl.splits, kv->num_kv_heads, batch);
+  p.persistent = pl.persistent;
+  const dim3 grid = pl.persistent ? dim3(pl.grid_x, 1, 1) : dim3(pl.splits, kv->num_kv_heads, batch);
   const cudaError_t e = kv->head_dim == 128 ? launch_verify<128>(pl, tk, tv, p, grid, stream)
                                              : launch_verify<64>(pl, tk, tv, p, grid, stream);
   return e == cudaSuccess ? VG_OK : VG_ERR_LAUNCH;
@@ -1093,14 +1282,14 @@ bool make_sparse_layout(int batch, int n_rows, int num_q_heads, int num_kv_heads
   // plan the splits over the largest union, as if it were a dense range
   const int eff = std::max(1, sl->u_max * kPageSize - n_rows);
   if (!make_verify_plan(batch, n_rows, num_q_heads, num_kv_heads, head_dim, eff, num_splits,
-                        &sl->pl))
+                        &sl->pl, true))
     return false;
   // a split's union pages must fit its shared-memory slice
   constexpr int kMaxTps = VerifyLayout<128>::kSliceMax / (kVTile / kPageSize);
   if (sl->pl.tiles_per_split > kMaxTps) {
     const int tiles = ceil_div(eff + n_rows, kVTile);
     if (!make_verify_plan(batch, n_rows, num_q_heads, num_kv_heads, head_dim, eff,
-                          std::max(num_splits, ceil_div(tiles, kMaxTps)), &sl->pl))
+                          std::max(num_splits, ceil_div(tiles, kMaxTps)), &sl->pl, true))
       return false;
     if (sl->pl.tiles_per_split > kMaxTps) return false;
   }

@@ -346,3 +346,64 @@ def test_full_size_workload(name):
         P.check_drafts_synthetic(st, inp, per_head, pairs=pairs, steps=[1, spec.n_drafts])
         del st
         torch.cuda.empty_cache()
+
+
+# More units (split x KV head x sequence) than SMs: persistent verify CTAs
+# each walk several units; ragged lengths give short last splits and
+# sequences with a single tile; M = g * R covers the 4-, 2- and 1-copy
+# layouts (96 rows: one softmax warp idle).
+PERSIST = dict(
+    ragged=dict(batch=4, prefix_lens=(3000, 9000, 1, 6001), num_q_heads=32, num_kv_heads=8,
+                top_k=200),
+    r8=dict(batch=3, prefix_lens=(4096, 4100, 2222), num_q_heads=32, num_kv_heads=8,
+            n_drafts=7),
+    m48=dict(batch=4, prefix_lens=(9000, 5000, 7777, 100), num_q_heads=16, num_kv_heads=2,
+             n_drafts=5),
+    m96=dict(batch=4, prefix_lens=(9000, 5000, 7777, 100), num_q_heads=16, num_kv_heads=2,
+             n_drafts=11),
+)
+
+
+@pytest.mark.parametrize("name", list(PERSIST))
+@pytest.mark.parametrize("mode", [1, 2, 3, 4])
+def test_persistent_verify(name, mode):
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    spec = small_spec(**PERSIST[name])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-(spec.max_prefix + spec.n_rows) // 128)
+    ran = 0
+    for ns in (40, 16, 71):  # 71: one-tile units
+        tps = -(-tiles // min(ns, tiles))
+        splits = -(-tiles // tps)
+        if spec.batch * spec.num_kv_heads * splits <= sms:
+            continue  # not the persistent path
+        ran += 1
+        inp, st = _run(spec, capture_mode=mode, num_splits=ns)
+        P.check_verify(st, inp)
+        rows64 = P.oracle_rows(inp) if mode != 4 else None
+        P.check_capture(st, inp, rows64)
+        P.check_select_end_to_end(st, inp, rows64)
+    assert ran >= 2
+
+
+def test_persistent_verify_skipped_sequence_and_repeat():
+    """A sequence whose length exceeds its bound is flagged and skipped by
+    the persistent CTAs; the others are unaffected, and a repeated call on a
+    NaN-poisoned workspace gives the same bits."""
+    _require_gpu()
+    from self_speculative_sparse_vg_gb300 import vg as V
+    from self_speculative_sparse_vg_gb300.workloads import small_spec
+    spec = small_spec(**PERSIST["ragged"])
+    inp, st = _run(spec, num_splits=40)
+    ref = st.out_verify.clone()
+    st.ws_verify.fill_(0xFF)
+    st.verify()
+    assert P.flag(st) == 0
+    assert torch.equal(st.out_verify, ref)
+    st.prefix_lens[2] = spec.max_prefix + 1
+    st.out_verify.fill_(0)
+    st.verify()
+    assert P.flag(st) & V.DEVERR_LENGTH
+    keep = [0, 1, 3]
+    assert torch.equal(st.out_verify[keep], ref[keep])
