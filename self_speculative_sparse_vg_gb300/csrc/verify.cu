@@ -140,12 +140,13 @@ struct VerifyBars {
   int stages;
 };
 
-// Q rows of a unit -> tensor-memory buffer `buf` (the A operand), by one
-// softmax warp for its 32 lanes: lane c * RPC + m holds packed row m of copy
-// c, every other lane zero (its logits are exactly zero).
+// Q rows of a unit for one softmax warp's 32 TMEM lanes (the A operand):
+// lane c * RPC + m holds packed row m of copy c, every other lane zero (its
+// logits are exactly zero).  load_q reads this lane's row into registers,
+// store_q writes them to tensor-memory buffer `buf`.
 template <int HD>
-__device__ __forceinline__ void write_q(const VerifyParams& p, uint32_t tmem, int buf, int b,
-                                        int h, int warp, int lane) {
+__device__ __forceinline__ void load_q(const VerifyParams& p, int b, int h, int warp, int lane,
+                                       uint4 (&x)[HD / 8]) {
   const int M = p.m_rows;
   const int CS = M <= 32 ? 4 : (M <= 64 ? 2 : 1);
   const int RPC = kMPad / CS;
@@ -158,12 +159,18 @@ __device__ __forceinline__ void write_q(const VerifyParams& p, uint32_t tmem, in
     src = reinterpret_cast<const uint4*>(
         p.q + ((size_t)(b * p.n_rows + i) * p.num_q_heads + h * p.group + qi) * HD);
   }
+#pragma unroll
+  for (int k = 0; k < HD / 8; ++k) x[k] = src ? src[k] : make_uint4(0, 0, 0, 0);
+}
+
+template <int HD>
+__device__ __forceinline__ void store_q(uint32_t tmem, int buf, int warp, const uint4 (&xq)[HD / 8]) {
   const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16) + kQCol + buf * (HD / 2);
 #pragma unroll
   for (int half = 0; half < HD / 64; ++half) {
     uint4 x[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = src ? src[half * 8 + k] : make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < 8; ++k) x[k] = xq[half * 8 + k];
     uint32_t v[32];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -178,6 +185,14 @@ __device__ __forceinline__ void write_q(const VerifyParams& p, uint32_t tmem, in
   tc_fence_before();
 }
 
+template <int HD>
+__device__ __forceinline__ void write_q(const VerifyParams& p, uint32_t tmem, int buf, int b,
+                                        int h, int warp, int lane) {
+  uint4 x[HD / 8];
+  load_q<HD>(p, b, h, warp, lane, x);
+  store_q<HD>(tmem, buf, warp, x);
+}
+
 // Softmax warp of a copy for one unit of work (a split of one KV head of one
 // sequence); COLS = 128 / CS columns of each tile, handled in chunks of 32
 // (two passes over TMEM when COLS > 32: maximum, then P).  `tbase` is the
@@ -185,11 +200,14 @@ __device__ __forceinline__ void write_q(const VerifyParams& p, uint32_t tmem, in
 // barrier phases follow that running count across units.  When the CTA has a
 // next unit (nb >= 0), its Q goes to tensor-memory buffer qbuf_next (arrival
 // on qfull[qbuf_next]) before this unit's epilogue, so that the tensor cores
-// can start its scores meanwhile.  `scratch` (the capture staging area, idle
-// by then) holds the copies' merge.
+// can start its scores meanwhile.  The copies' merge goes through `scratch`
+// (the capture staging area, idle by then) one 32-column chunk at a time, or
+// through the ring all at once when `ring` is given (a CTA's only unit: no
+// load is in flight at its epilogue).
 template <int HD, int COLS, int CM, bool SP>
 __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const VerifyBars& bars,
-                                               float* scratch, float* cap_s, float* all_s,
+                                               float* scratch, float* ring, float* cap_s,
+                                               float* all_s,
                                                const int32_t* sl_page, const uint32_t* sl_mask,
                                                int sl_n, uint32_t tmem, int b, int h, int split,
                                                int t0, int ntiles, int L, int tbase, int& hs,
@@ -432,10 +450,11 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
                       ((tbase + ntiles - 1) / stages) & 1, p.wait_ns, p.error_flag);
   tc_fence_after();
   // scratch, column-major so that a warp's 32 rows are 32 consecutive
-  // floats: sml[copy - 1][{m, l}][row], then one 32-column chunk of O per
-  // copy so[copy - 1][d][row]
+  // floats: sml[copy - 1][{m, l}][row], then W columns of O per copy
+  // so[copy - 1][d][row] (W = 32, or all of head_dim through the ring)
   float* sml = scratch;
-  float* so = scratch + (CS > 1 ? (CS - 1) * 2 * RPC : 0);
+  const int per = ring ? HD / 32 : 1;  // 32-column chunks per hand-over
+  float* so = ring ? ring : scratch + (CS > 1 ? (CS - 1) * 2 * RPC : 0);
   if (CS > 1 && c > 0) {
     sml[((c - 1) * 2) * RPC + m] = m_used;
     sml[((c - 1) * 2 + 1) * RPC + m] = lsum;
@@ -458,28 +477,42 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
   const size_t bh = (size_t)b * p.num_kv_heads + h;
   const float inv = lt_all > 0.f ? 1.f / lt_all : 0.f;
 #pragma unroll 1
-  for (int cc = 0; cc < HD / 32; ++cc) {
-    float o[32];
-    if (ntiles > 0) {
-      tmem_ld32(trow + kOCol + cc * 32, o);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 32; ++k) o[k] = 0.f;
-    }
-    if (CS > 1) {  // copies 1.. hand their chunk to copy 0
+  for (int g0 = 0; g0 < HD / 32; g0 += per) {
+    if (CS > 1) {  // copies 1.. hand their columns to copy 0
       if (c > 0) {
-        float* d = so + (size_t)(c - 1) * 32 * RPC + m;
+#pragma unroll 1
+        for (int cc = g0; cc < g0 + per; ++cc) {
+          float o[32];
+          if (ntiles > 0) {
+            tmem_ld32(trow + kOCol + cc * 32, o);
+          } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) d[k * RPC] = o[k];
+            for (int k = 0; k < 32; ++k) o[k] = 0.f;
+          }
+          float* d = so + ((size_t)(c - 1) * per + (cc - g0)) * 32 * RPC + m;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) d[k * RPC] = o[k];
+        }
       }
       named_barrier_sync(1, 4 * 32);
+    }
+#pragma unroll 1
+  for (int cc = g0; cc < g0 + per; ++cc) {
+    float o[32];
+    if (c == 0) {
+      if (ntiles > 0) {
+        tmem_ld32(trow + kOCol + cc * 32, o);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] = 0.f;
+      }
     }
     if (c == 0 && m < M) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) o[k] *= w0;
 #pragma unroll
       for (int c2 = 1; c2 < CS; ++c2) {
-        const float* src = so + (size_t)(c2 - 1) * 32 * RPC + m;
+        const float* src = so + ((size_t)(c2 - 1) * per + (cc - g0)) * 32 * RPC + m;
 #pragma unroll
         for (int k = 0; k < 32; ++k) o[k] += wc[c2 - 1] * src[k * RPC];
       }
@@ -502,7 +535,10 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
           *reinterpret_cast<float4*>(dst + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
       }
     }
-    if (CS > 1) named_barrier_sync(1, 4 * 32);  // the chunk is read before the next is written
+  }
+    // the columns are read before the next are written, and before any warp
+    // goes on to the next unit (whose capture staging overlaps the scratch)
+    if (CS > 1) named_barrier_sync(1, 4 * 32);
   }
   if (c > 0) return;
   if (m < M && p.splits > 1) {
@@ -689,6 +725,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
     }
   }
 
+  // the first unit's Q rows: loads issued now, written to tensor memory once
+  // it is allocated
+  uint4 qreg[HD / 8];
+  if (warp < 4) load_q<HD>(p, b0, h0, warp, lane, qreg);
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&bars.kfull[s], 1);
@@ -719,7 +760,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   // named barrier 2 (warps 0-3 and 5); later units' Q through qfull.
   constexpr int kQReadyBar = 2, kQReadyThreads = 5 * 32;
   if (warp < 4) {
-    write_q<HD>(p, tmem, 0, b0, h0, warp, lane);
+    store_q<HD>(tmem, 0, warp, qreg);
     if (n_units > 1) write_q<HD>(p, tmem, 1, -1, 0, warp, lane);
     named_barrier_sync(kQReadyBar, kQReadyThreads);
   } else if (warp == kMmaWarp) {
@@ -933,6 +974,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
   } else if (warp < NAW) {
     // ---------------------------------------------------------- softmax
     float* scratch = cap_s;  // the capture staging and slice area, idle in an epilogue
+    // a CTA with one unit has an idle ring at its epilogue
+    float* ring_f = n_units == 1 ? reinterpret_cast<float*>(ring) : nullptr;
     int tbase = 0, hs = 0;
     for (int k = 0; k < n_units; ++k) {
       int b, h, split, t0, ntiles, L;
@@ -941,11 +984,11 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
       unit_of(k + 1, nb, nh, nsplit, nt0n, nntiles, nL);
       const int qn = (k + 1) & 1;
       if (CS == 4)
-        verify_softmax<HD, 32, CM, SP>(p, bars, scratch, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
+        verify_softmax<HD, 32, CM, SP>(p, bars, scratch, ring_f, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
       else if (CS == 2)
-        verify_softmax<HD, 64, CM, SP>(p, bars, scratch, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
+        verify_softmax<HD, 64, CM, SP>(p, bars, scratch, ring_f, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
       else
-        verify_softmax<HD, 128, CM, SP>(p, bars, scratch, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
+        verify_softmax<HD, 128, CM, SP>(p, bars, scratch, ring_f, cap_s, all_s, sl_page, sl_mask, sl_n, tmem, b, h, split, t0, ntiles, L, tbase, hs, nb, nh, qn, warp, lane);
       tbase += ntiles;
     }
   }
