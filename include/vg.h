@@ -228,11 +228,21 @@ vg_status vg_sparse_verify_attention(const vg_paged_kv* kv, const void* q,
  *            row); no initialisation needed.
  * The call launches one thread-block-cluster selection kernel on `stream`,
  * preceded by a score kernel that writes the keys to the workspace when the
- * cluster would have many capture loads per CTA (long prefixes, raw-row and
- * attention-weight captures).
+ * cluster would have many capture loads per CTA (long prefixes, large
+ * batches, raw-row and attention-weight captures); vg_select_launches() says
+ * which.
  * Supported: max_prefix <= 262144, num_q_heads / num_kv_heads <= 8.
  * ------------------------------------------------------------------------- */
 size_t vg_select_workspace_bytes(int batch, int num_kv_heads, int max_prefix, int per_head);
+
+/* Kernels one vg_select_kv (capture_mode VG_CAPTURE_GROUP_SUM, _ALL_SUM or
+ * _ROWS) or vg_select_kv_weights (VG_CAPTURE_ALL_ROWS) call launches for this
+ * shape on the current device: 1 (the selection cluster forms the keys
+ * itself) or 2 (a score kernel first).  The cluster size depends on how many
+ * clusters the device holds at once, so the answer is device-specific.
+ * Returns 0 for an invalid or unsupported shape.  Launches nothing. */
+int vg_select_launches(int capture_mode, int batch, int num_kv_heads, int max_prefix,
+                       int per_head);
 
 vg_status vg_select_kv(const float* capture, int capture_mode, const int32_t* prefix_lens,
                        int batch, int num_q_heads, int num_kv_heads, int max_prefix, int top_k,

@@ -9,10 +9,12 @@
 // Design: one thread-block cluster of C (<= 16) CTAs per selection row; CTA c
 // owns a contiguous slice of positions.  Each position's fp32 score is formed
 // in the documented order and turned into an order-preserving 32-bit key:
-// for the per-KV-head sum captures, when a CTA's share is at most 16K loads,
+// for the per-KV-head sum captures, when a CTA's share is at most 32K loads,
 // by the cluster's CTAs themselves, straight into shared memory; otherwise
 // (longer prefixes, raw-row and attention-weight captures) by a score kernel
-// spread over many CTAs, through the workspace.  The cluster then runs an
+// spread over many CTAs, through the workspace.  Clusters are halved (longer
+// slices) while a batch's clusters would not all be resident at once: a
+// second wave of clusters costs as much as the first.  The cluster then runs an
 // MSB-first 8-bit radix select (at most 4 passes, fewer once the whole
 // boundary bin is kept): every CTA pushes its 256-bin histogram into every
 // CTA's shared memory with st.async, each CTA waits on a local mbarrier for
@@ -23,6 +25,10 @@
 // The result is deterministic and equals a stable sort by (score desc,
 // position asc).
 #include <cooperative_groups.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "vg_device.cuh"
 #include "vg_host.h"
@@ -36,7 +42,7 @@ constexpr int kSelThreads = 1024;
 constexpr int kMaxCluster = 16;
 constexpr int kTargetSlice = 2048;
 constexpr int kMaxSlice = 16384;  // keys per CTA (64 KB of shared memory)
-constexpr int kFusedLoads = 16384;  // capture loads per CTA up to which the cluster scores
+constexpr int kFusedLoads = 32768;  // capture loads per CTA up to which the cluster scores
 
 struct SelectParams {
   const float* capture;
@@ -239,7 +245,32 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   bool peers_ready = false;
 
   if (tid < 256) hist[0][tid] = 0;  // the first pass's histogram
-  if (p.fused) {
+  const int terms = p.per_head ? 1 : p.num_kv_heads;
+  if (p.fused && terms <= 8) {
+    // four positions per thread at a time (coalesced across the threads),
+    // every capture load of the four issued before the first add
+    const size_t Lm = p.max_prefix;
+    const float* G = p.capture + (size_t)b * p.num_kv_heads * Lm + (p.per_head ? (size_t)row * Lm : 0);
+    for (int j0 = tid; j0 < n_loc; j0 += 4 * kSelThreads) {
+      float v[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kSelThreads;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          v[u][t] = (t < terms && j < n_loc) ? __ldg(G + (size_t)t * Lm + lo + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kSelThreads;
+        float acc = v[u][0];
+#pragma unroll
+        for (int t = 1; t < 8; ++t)
+          if (t < terms) acc = acc + v[u][t];
+        if (j < n_loc) keys[j] = score_key(acc);
+      }
+    }
+  } else if (p.fused) {
 #pragma unroll 2
     for (int j = tid; j < n_loc; j += blockDim.x)
       keys[j] = score_key(group_sum_score(p, b, row, lo + j));
@@ -471,14 +502,79 @@ size_t select_smem_bytes(int slice) {
          align_up(((size_t)slice / 16 + 2) * 4, 16);
 }
 
-bool select_shape(int max_prefix, int* C, int* slice) {
+bool set_select_attributes() {
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && done[dev]) return true;
+  if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)select_smem_bytes(kMaxSlice)) != cudaSuccess ||
+      cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess)
+    return false;
+  if (dev < 64) done[dev] = true;
+  return true;
+}
+
+// Clusters of C CTAs (slice of `slice` keys each) the device holds at once.
+int select_max_clusters(int C, int slice) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, int> memo;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, C, slice);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    const auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, 1, 1);
+  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.dynamicSmemBytes = select_smem_bytes(slice);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, select_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> g(mu);
+  memo[key] = n;
+  return n;
+}
+
+// Cluster size and keys per CTA for `clusters` selection rows of max_prefix
+// positions: slices of about kTargetSlice keys in clusters of up to
+// kMaxCluster CTAs, halved while the rows' clusters would not all be resident
+// at once (a second wave costs a whole selection) and the slice still fits.
+bool select_shape(int max_prefix, long long clusters, int* C, int* slice) {
   int c = 1;
   while (c < kMaxCluster && ceil_div(max_prefix, c) > kTargetSlice) c *= 2;
-  const int s = align_up(ceil_div(max_prefix, c), 4);
+  int s = align_up(ceil_div(max_prefix, c), 4);
   if (s > kMaxSlice) return false;
+  while (c > 1) {
+    const int s2 = align_up(ceil_div(max_prefix, c / 2), 4);
+    if (s2 > kMaxSlice || clusters <= 1 || clusters <= select_max_clusters(c, s)) break;
+    c /= 2;
+    s = s2;
+  }
   *C = c;
   *slice = s;
   return true;
+}
+
+// Whether the cluster forms the keys itself (no score kernel): per-KV-head sum
+// captures whose CTAs have few loads to issue (up to kFusedLoads each);
+// otherwise the score kernel spreads the loads over the whole device.
+bool select_fused(int capture_mode, int per_head, int num_kv_heads, int slice) {
+  return capture_mode == VG_CAPTURE_GROUP_SUM &&
+         (long long)(per_head ? 1 : num_kv_heads) * slice <= kFusedLoads;
 }
 
 }  // namespace
@@ -499,6 +595,19 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
                              int n_recent, int per_head, int32_t* indices, int32_t* counts,
                              int cap, const vg_paged_kv* kv, int32_t* slots, void* workspace,
                              size_t workspace_bytes, int32_t* error_flag, cudaStream_t stream);
+
+extern "C" int vg_select_launches(int capture_mode, int batch, int num_kv_heads, int max_prefix,
+                                  int per_head) {
+  if (batch <= 0 || num_kv_heads <= 0 || max_prefix <= 0) return 0;
+  if (capture_mode == VG_CAPTURE_ALL_SUM) capture_mode = VG_CAPTURE_GROUP_SUM;
+  if (capture_mode != VG_CAPTURE_GROUP_SUM && capture_mode != VG_CAPTURE_ROWS &&
+      capture_mode != VG_CAPTURE_ALL_ROWS)
+    return 0;
+  int C, slice;
+  if (!select_shape(max_prefix, 1, &C, &slice) || !set_select_attributes()) return 0;
+  select_shape(max_prefix, (long long)batch * (per_head ? num_kv_heads : 1), &C, &slice);
+  return select_fused(capture_mode, per_head, num_kv_heads, slice) ? 1 : 2;
+}
 
 extern "C" vg_status vg_select_kv(const float* capture, int capture_mode,
                                   const int32_t* prefix_lens, int batch, int num_q_heads,
@@ -549,9 +658,11 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
   const long long budget = (long long)n_sink + n_recent + top_k;
   if (cap < std::min<long long>(max_prefix, budget)) return VG_ERR_INVALID_ARGUMENT;
   int C, slice;
-  if (!select_shape(max_prefix, &C, &slice)) return VG_ERR_UNSUPPORTED;
+  if (!select_shape(max_prefix, 1, &C, &slice)) return VG_ERR_UNSUPPORTED;
   const size_t ws_need = vg_select_workspace_bytes(batch, num_kv_heads, max_prefix, per_head);
   if (!workspace || workspace_bytes < ws_need) return VG_ERR_WORKSPACE_TOO_SMALL;
+  if (!set_select_attributes()) return VG_ERR_LAUNCH;
+  select_shape(max_prefix, (long long)batch * (per_head ? num_kv_heads : 1), &C, &slice);
 
   SelectParams p;
   p.capture = capture;
@@ -580,24 +691,8 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
   p.wait_ns = wait_report_ns();
   p.rows = per_head ? num_kv_heads : 1;
   p.slice = slice;
-  // the cluster forms the keys itself when its CTAs have few loads to issue
-  // (up to kFusedLoads per CTA); otherwise the score kernel spreads them
-  p.fused = capture_mode == VG_CAPTURE_GROUP_SUM &&
-                    (long long)(per_head ? 1 : num_kv_heads) * slice <= kFusedLoads
-                ? 1
-                : 0;
+  p.fused = select_fused(capture_mode, per_head, num_kv_heads, slice) ? 1 : 0;
 
-  static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)select_smem_bytes(kMaxSlice)) != cudaSuccess ||
-        cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess)
-      return VG_ERR_LAUNCH;
-    attr_done[dev] = true;
-  }
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;

@@ -257,11 +257,12 @@ class DecodeStack:
     def launches_per_iteration(self) -> int:
         """Kernels per layer and draft/verify iteration: k drafts, the verify
         (+ split merge) and the selection."""
-        from .step import select_launches
         s = self.spec
         merge = 1 if self.ws_verify[self.R].numel() > 1 else 0
-        return s.n_drafts + 1 + merge + select_launches(vg.CAPTURE_GROUP_SUM, s.per_head,
-                                                        s.num_kv_heads, s.max_prefix)
+        with torch.cuda.device(self.device):
+            sel = vg.select_launches(vg.CAPTURE_GROUP_SUM, s.batch, s.num_kv_heads, s.max_prefix,
+                                     s.per_head)
+        return s.n_drafts + 1 + merge + sel
 
     def run(self, iterations: Optional[int] = None):
         self.seed_selection()

@@ -159,20 +159,7 @@ class DecodeStep:
         than one split), the selection's kernels, one kernel per draft step."""
         merge = 1 if self.ws_verify.numel() > 1 else 0
         sp = self.spec
-        return (1 + merge + select_launches(self.capture_mode, self.per_head, sp.num_kv_heads,
-                                            sp.max_prefix) + sp.n_drafts)
-
-
-def select_launches(capture_mode, per_head, num_kv_heads, max_prefix) -> int:
-    """Kernels vg_select_kv launches, restating the library's rule: one
-    cluster of up to 16 CTAs per selection row takes slices of at least 2048
-    positions; the cluster forms the score keys itself for per-KV-head sum
-    captures when a CTA has at most 16384 capture loads, otherwise a score
-    kernel runs first."""
-    c = 1
-    while c < 16 and -(-max_prefix // c) > 2048:
-        c *= 2
-    slice_ = (-(-max_prefix // c) + 3) // 4 * 4
-    fused = capture_mode in (vg.CAPTURE_GROUP_SUM, vg.CAPTURE_ALL_SUM) and \
-        (1 if per_head else num_kv_heads) * slice_ <= 16384
-    return 1 if fused else 2
+        with torch.cuda.device(self.device):
+            sel = vg.select_launches(self.capture_mode, sp.batch, sp.num_kv_heads, sp.max_prefix,
+                                     self.per_head)
+        return 1 + merge + sel + sp.n_drafts

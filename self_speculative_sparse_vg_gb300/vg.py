@@ -29,7 +29,7 @@ DEVERR_LENGTH = 16
 
 EXPORTED = (
     "vg_verify_workspace_bytes", "vg_verify_attention",
-    "vg_select_workspace_bytes", "vg_select_kv", "vg_select_kv_weights",
+    "vg_select_workspace_bytes", "vg_select_launches", "vg_select_kv", "vg_select_kv_weights",
     "vg_sparse_draft_workspace_bytes", "vg_sparse_draft_attention",
     "vg_status_string", "vg_version",
     "vg_verify_noalloc_scratch_bytes", "vg_verify_attention_noalloc",
@@ -63,6 +63,7 @@ def _load():
         "vg_verify_attention": (i32, [kvp, vp, vp, i32, i32, i32, i32, f32, vp, i32, vp, i32,
                                       vp, sz, vp, vp]),
         "vg_select_workspace_bytes": (sz, [i32, i32, i32, i32]),
+        "vg_select_launches": (i32, [i32, i32, i32, i32, i32]),
         "vg_select_kv_weights": (i32, [vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp,
                                        vp, i32, kvp, vp, vp, sz, vp, vp]),
         "vg_select_kv": (i32, [vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, i32,
@@ -213,6 +214,13 @@ def sparse_verify_attention(kv: PagedKV, q, prefix_lens, max_prefix, softmax_sca
 # --------------------------------------------------------------------- select
 def select_workspace_bytes(batch, num_kv_heads, max_prefix, per_head) -> int:
     return int(_lib.vg_select_workspace_bytes(batch, num_kv_heads, max_prefix, int(bool(per_head))))
+
+
+def select_launches(capture_mode, batch, num_kv_heads, max_prefix, per_head) -> int:
+    """Kernels one selection call launches for this shape on the current
+    device (1 or 2; 0 for an unsupported shape)."""
+    return int(_lib.vg_select_launches(int(capture_mode), batch, num_kv_heads, max_prefix,
+                                       int(bool(per_head))))
 
 
 def _kv_arg(kv, slots):

@@ -101,6 +101,10 @@ def test_host_argument_checks_without_gpu():
                           None, None, 0, None, None) == 1
     assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 300000, 100, 4, 16, 0, fake, fake, 200, None,
                           None, None, 0, None, None) == 2
+    # select: launch count of an invalid or unsupported shape (no device needed)
+    assert L.vg_select_launches(0, 0, 8, 5000, 0) == 0
+    assert L.vg_select_launches(0, 1, 8, 300000, 0) == 0
+    assert L.vg_select_launches(7, 1, 8, 5000, 0) == 0
     # select: the score-key workspace is missing or too small
     assert L.vg_select_workspace_bytes(1, 8, 5000, 0) >= 5000 * 4
     assert L.vg_select_kv(fake, 1, fake, 1, 32, 8, 5000, 100, 4, 16, 0, fake, fake, 200, None,
