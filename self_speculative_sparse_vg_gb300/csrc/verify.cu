@@ -33,6 +33,7 @@
 //    workspace; a small merge kernel, one CTA per (output row, KV head,
 //    sequence), combines them.  It is chained with programmatic dependent
 //    launch, so its launch overlaps the verify grid.
+#include <climits>
 #include <mutex>
 
 #include "vg_device.cuh"
@@ -795,24 +796,35 @@ __global__ void __launch_bounds__(kVerifyThreads, 1)
       }
       const int npages_b = (L + R + kPageSize - 1) / kPageSize;
       const int tbase = k_armed;
-      // page ids of tiles [4w, 4w + 4) for the window w of the K tile, and of
-      // the window before it (V runs one tile behind)
+      // Page ids of tiles [4w, 4w + 4) for the window w of the K tile, and of
+      // the window before it (V runs one tile behind).  The page-table entries
+      // of window w + 1 are read when window w starts, so that the load's
+      // latency is hidden behind four tiles of streaming.
+      constexpr int kNoPage = INT_MIN;  // lane's slot lies outside the unit
+      auto fetch = [&](int kt) -> int {
+        const int lt_l = kt + (lane >> 3);
+        const int slot = lt_l * kPagesPerTile + (lane & 7);
+        const int lp = SP ? (slot < sl_n ? sl_page[slot] : -1)
+                          : (t0 + lt_l) * kPagesPerTile + (lane & 7);
+        if (lt_l < ntiles && lp >= 0 && lp < npages_b)
+          return (kt == 0 && !SP) ? pre_id : p.page_table[(size_t)b * p.max_pages_per_seq + lp];
+        return kNoPage;
+      };
+      int raw_now = fetch(0), raw_ahead = fetch(4);
       int id_cur = p.num_pages, id_prev = p.num_pages;
       for (int kt = 0; kt <= ntiles; ++kt) {
         const int vt = kt - 1;
         const bool new_window = kt < ntiles && (kt & 3) == 0;
         if (new_window) {
           id_prev = id_cur;
-          const int lt_l = kt + (lane >> 3);
-          const int slot = lt_l * kPagesPerTile + (lane & 7);
-          const int lp = SP ? (slot < sl_n ? sl_page[slot] : -1)
-                            : (t0 + lt_l) * kPagesPerTile + (lane & 7);
+          if (kt > 0) {
+            raw_now = raw_ahead;
+            raw_ahead = fetch(kt + 4);
+          }
           id_cur = p.num_pages;  // out of range: TMA fills zeros
-          if (lt_l < ntiles && lp >= 0 && lp < npages_b) {
-            const int e = (kt == 0 && !SP) ? pre_id
-                                           : p.page_table[(size_t)b * p.max_pages_per_seq + lp];
-            if (e >= 0 && e < p.num_pages)
-              id_cur = e;
+          if (raw_now != kNoPage) {
+            if (raw_now >= 0 && raw_now < p.num_pages)
+              id_cur = raw_now;
             else
               flag_error(p.error_flag, VG_DEVERR_PAGE);
           }
