@@ -32,10 +32,7 @@
  *     arguments on the same device (0 = none needed, the pointer may be
  *     NULL).  Calls that share a workspace must not overlap in time.  The
  *     verify and select workspaces need no initialisation: everything in
- *     them is written before it is read.  The sparse-draft workspace starts
- *     with completion counters that must be zero before its first use
- *     (cudaMemsetAsync once after allocating it); every call leaves them
- *     zero again.
+ *     them is written before it is read.  The sparse draft needs none.
  */
 #ifndef VG_H_
 #define VG_H_
@@ -291,14 +288,13 @@ vg_status vg_select_kv_weights(const float* capture, int n_rows, const int32_t* 
  *               rows are always reached through the page table.
  *   out         bf16 [batch][num_q_heads][head_dim]; zero when nothing is
  *               attended (count 0 and an empty tail).
- *   workspace   vg_sparse_draft_workspace_bytes(); zero-filled before its
- *               first use (see the conventions above).  If a call flags
- *               VG_DEVERR_TIMEOUT, zero it again before the next call.
+ *   workspace   none needed: vg_sparse_draft_workspace_bytes() returns 0;
+ *               the pointer and size are ignored (they may be NULL / 0).
  * One kernel: the attended list (selection, then tail) is processed in
- * chunks of 128 entries, one CTA each.  A list of one chunk writes `out`
- * directly; otherwise every chunk writes an fp32 record (m, l, O) to the
- * workspace and the chunk that completes a (sequence, KV head) merges them
- * into `out`.
+ * chunks of 64 entries, cut into up to 16 segments, one CTA each; the
+ * segments of a (sequence, KV head) form one thread-block cluster and their
+ * fp32 records (m, l, O) are merged by the cluster's first CTA through
+ * distributed shared memory, which writes `out`.
  * Supported: head_dim 64/128, g in [1, 8], cap + max_tail <= 65536.
  * ------------------------------------------------------------------------- */
 size_t vg_sparse_draft_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,

@@ -95,22 +95,54 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Waits whose completion is acquired at cluster scope: for a phase that
+// another CTA of the cluster completes with a release at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity.  Past report_ns the wait ORs
 // VG_DEVERR_TIMEOUT into *flag and keeps waiting; it returns false (also
 // flagged) only when kWaitLimitNs has passed as well.  Under a bound shorter
 // than the default it polls with the non-blocking test and reads the timer
 // after every poll (a try_wait may itself sleep past a short bound).
+// CLUSTER: acquire at cluster scope (see mbar_try_wait_cluster).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_checked(uint64_t* bar, uint32_t parity,
                                                   uint64_t report_ns, int32_t* flag) {
   const bool short_bound = report_ns < kWaitLimitNs;
-  if (short_bound ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() {
+    if (CLUSTER)
+      return short_bound ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity);
+    return short_bound ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
   const uint64_t t0 = global_timer_ns();
   const int polls = short_bound ? 1 : 32;
   bool reported = false;
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < polls; ++i)
-      if (short_bound ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+      if (poll()) return true;
     const uint64_t dt = global_timer_ns() - t0;
     if (!reported && (dt > report_ns || dt > kWaitLimitNs)) {
       flag_error(flag, VG_DEVERR_TIMEOUT);
@@ -140,6 +172,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rb
           "r"(raddr),
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
       : "memory");
+}
+// Arrive once on the mbarrier at shared::cluster address `rbar` (possibly in
+// another CTA), releasing this thread's prior memory accesses at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar)
+               : "memory");
 }
 // Split cluster barrier (every thread of every CTA arrives, then waits).
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -260,9 +298,28 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
+// 16-byte copy that reads src_bytes (0 or 16) bytes and zero-fills the rest.
+__device__ __forceinline__ void cp_async_16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// cp_async_wait with a run-time count (0 .. 7; more waits as for 7).
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+  }
 }
 
 // ------------------------------------------------- tcgen05 (5th-gen tensor cores)

@@ -288,8 +288,8 @@ def sparse_draft_attention(kv: PagedKV, q, indices, counts, per_head, tail_start
                            max_tail, softmax_scale, out, workspace=None, error_flag=None,
                            stream=None, slots=None):
     """vg_sparse_draft_attention.  q [B][Hq][d] bf16; slots (optional) as
-    written by select_kv beside the indices.  The workspace must be
-    zero-filled before its first use (zero_workspace does that)."""
+    written by select_kv beside the indices.  No workspace is needed (the
+    argument is accepted and ignored)."""
     B, Hq, _ = q.shape
     st = kv.struct()
     cap = indices.shape[-1]
@@ -305,7 +305,7 @@ def sparse_draft_attention(kv: PagedKV, q, indices, counts, per_head, tail_start
 
 
 def zero_workspace(nbytes: int, device) -> torch.Tensor:
-    """A zero-filled byte workspace.  The sparse-draft workspace needs it (its
-    completion counters start at zero); for the others zeros only keep a
-    fresh buffer free of stale bytes."""
+    """A zero-filled byte workspace of at least one byte (zeros only keep a
+    fresh buffer free of stale bytes: every workspace is written before it
+    is read)."""
     return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
