@@ -50,9 +50,8 @@
 namespace vg {
 namespace {
 
-constexpr int kChunk = 64;           // attended entries per chunk
-constexpr int kWarps = kChunk / 16;  // one warp per 16 entries
-constexpr int kThreads = kWarps * 32;
+// A CTA has W warps (4 or 8, planned per launch) and takes chunks of 16 W
+// attended entries: warp w computes entries [16w, 16w + 16) of each chunk.
 constexpr int kMinStages = 2;        // chunks in flight per CTA: 2 .. kMaxStages, planned
 constexpr int kMaxStages = 6;
 constexpr int kMaxEntries = 65536;   // cap + max_tail
@@ -81,8 +80,10 @@ struct DraftParams {
   float scale_log2;
 };
 
-template <int HD>
+template <int HD, int W>
 struct DraftLayout {
+  static constexpr int kChunk = 16 * W;                    // attended entries per chunk
+  static constexpr int kThreads = 32 * W;
   static constexpr int kRowBytes = HD * 2 + 16;            // padded K / V row
   static constexpr int kTileBytes = kChunk * kRowBytes;    // one of K / V of a chunk
   static constexpr int kStageBytes = 2 * kTileBytes;
@@ -92,7 +93,13 @@ struct DraftLayout {
     return 128 + (size_t)stages * kStageBytes + (slots ? 0 : (size_t)kPtMax * 4) + 64;
   }
   static constexpr int kRecBytes = (kRecHead + 8 * HD) * 4;  // one record at g = 8
-  static_assert((size_t)kWarps * (HD / 8) * kOStride * 4 <= (size_t)kMinRing,
+  // deepest ring that fits 227 KB with the page-table row and static memory
+  static constexpr int kStagesFit =
+      (227 * 1024 - 6 * 1024 - 192 - kPtMax * 4) / kStageBytes < kMaxStages
+          ? (227 * 1024 - 6 * 1024 - 192 - kPtMax * 4) / kStageBytes
+          : kMaxStages;
+  static_assert(kStagesFit >= kMinStages, "two stages fit");
+  static_assert((size_t)W * (HD / 8) * kOStride * 4 <= (size_t)kMinRing,
                 "the O stash reuses the ring");
   static_assert((size_t)(kMaxSegments - 1) * kRecBytes <= (size_t)kMinRing,
                 "the leader receives the other segments' records in its ring");
@@ -157,10 +164,11 @@ __device__ __forceinline__ int entry_row(const DraftParams& p, const int32_t* pt
 // cp.async pieces, consecutive lanes on consecutive pieces of a row.  A row
 // without an entry is zero-filled (source size 0).  The pieces form one
 // cp.async group per chunk.
-template <int HD>
+template <int HD, int W>
 __device__ __forceinline__ void gather_chunk(const DraftParams& p, int row, int* row_s,
                                              uint8_t* stage) {
-  using Lay = DraftLayout<HD>;
+  using Lay = DraftLayout<HD, W>;
+  constexpr int kChunk = Lay::kChunk, kThreads = Lay::kThreads;
   constexpr int RB = Lay::kRowBytes;
   constexpr int PR = HD * 2 / 16;  // pieces per row
   const int t = threadIdx.x;
@@ -187,9 +195,10 @@ __device__ __forceinline__ int seg_bound(int r, int S, int chunks) {
   return (int)(((long long)chunks * w) / (2 * S - 1));
 }
 
-template <int HD, bool SLOTS>
-__global__ void __launch_bounds__(kThreads) sparse_draft_kernel(const DraftParams p) {
-  using Lay = DraftLayout<HD>;
+template <int HD, bool SLOTS, int W>
+__global__ void __launch_bounds__(32 * W) sparse_draft_kernel(const DraftParams p) {
+  using Lay = DraftLayout<HD, W>;
+  constexpr int kChunk = Lay::kChunk, kThreads = Lay::kThreads, kWarps = W;
   constexpr int KS = HD / 16;  // k-steps of Q K^T
   constexpr int DN = HD / 8;   // O n-tiles
   constexpr int RB = Lay::kRowBytes;
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(kThreads) sparse_draft_kernel(const DraftParam
         const int rw = tid < kChunk ? entry_row<SLOTS>(p, pt_s, pt_in_smem, b, h, c * kChunk + tid,
                                                        n_att, cnt, ts, pos_n[s], slot_n[s])
                                     : -1;
-        gather_chunk<HD>(p, rw, row_s[s], ring + s * Lay::kStageBytes);
+        gather_chunk<HD, W>(p, rw, row_s[s], ring + s * Lay::kStageBytes);
       } else if (s < stages) {
         cp_async_commit();  // an empty group: every chunk has stages - 1 groups after its own
       }
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(kThreads) sparse_draft_kernel(const DraftParam
         const int rw = tid < kChunk ? entry_row<SLOTS>(p, pt_s, pt_in_smem, b, h, cn * kChunk + tid,
                                                        n_att, cnt, ts, pos_nx, slot_nx)
                                     : -1;
-        gather_chunk<HD>(p, rw, row_s[st], ring + st * Lay::kStageBytes);
+        gather_chunk<HD, W>(p, rw, row_s[st], ring + st * Lay::kStageBytes);
       } else {
         cp_async_commit();
       }
@@ -601,32 +610,35 @@ __global__ void __launch_bounds__(kThreads) sparse_draft_kernel(const DraftParam
 }
 
 // CTAs of the draft kernel resident per SM with a ring of `stages` stages
-// (cached per device, variant and stages); also sets the kernel's dynamic
-// shared-memory limit and allows clusters of up to 16 CTAs, once per device.
-template <int HD, bool SLOTS>
+// (cached per device, variant and stages; -1 when the ring does not fit);
+// also sets the kernel's dynamic shared-memory limit and allows clusters of
+// up to 16 CTAs, once per device.
+template <int HD, bool SLOTS, int W>
 int draft_occupancy(int stages) {
+  using Lay = DraftLayout<HD, W>;
   static int cached[64][kMaxStages + 1] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || stages < kMinStages ||
-      stages > kMaxStages)
+      stages > Lay::kStagesFit)
     return -1;
   std::lock_guard<std::mutex> lock(mu);
   if (cached[dev][0] == 0) {
     const bool ok =
-        cudaFuncSetAttribute(sparse_draft_kernel<HD, SLOTS>,
+        cudaFuncSetAttribute(sparse_draft_kernel<HD, SLOTS, W>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)DraftLayout<HD>::bytes(SLOTS, kMaxStages)) == cudaSuccess &&
-        cudaFuncSetAttribute(sparse_draft_kernel<HD, SLOTS>,
+                             (int)Lay::bytes(SLOTS, Lay::kStagesFit)) == cudaSuccess &&
+        cudaFuncSetAttribute(sparse_draft_kernel<HD, SLOTS, W>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
     cached[dev][0] = ok ? 1 : -1;
   }
   if (cached[dev][0] < 0) return -1;
   if (cached[dev][stages] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, sparse_draft_kernel<HD, SLOTS>, kThreads,
-            DraftLayout<HD>::bytes(SLOTS, stages)) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_draft_kernel<HD, SLOTS, W>,
+                                                      Lay::kThreads,
+                                                      Lay::bytes(SLOTS, stages)) != cudaSuccess ||
+        n <= 0)
       n = -1;
     cached[dev][stages] = n;
   }
@@ -635,21 +647,22 @@ int draft_occupancy(int stages) {
 
 // Clusters of S draft CTAs (ring of `stages` stages) the device holds at
 // once (cached per device, variant, S and stages).
-template <int HD, bool SLOTS>
+template <int HD, bool SLOTS, int W>
 int draft_max_clusters(int S, int stages) {
+  using Lay = DraftLayout<HD, W>;
   static int cached[64][kMaxSegments + 1][kMaxStages + 1] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || S < 1 || S > kMaxSegments ||
-      stages < kMinStages || stages > kMaxStages)
+      stages < kMinStages || stages > Lay::kStagesFit)
     return 0;
   std::lock_guard<std::mutex> lock(mu);
   int& c = cached[dev][S][stages];
   if (c == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = DraftLayout<HD>::bytes(SLOTS, stages);
+    cfg.blockDim = dim3(Lay::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Lay::bytes(SLOTS, stages);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = S;
@@ -658,7 +671,8 @@ int draft_max_clusters(int S, int stages) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, sparse_draft_kernel<HD, SLOTS>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_draft_kernel<HD, SLOTS, W>, &cfg) !=
+        cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -671,26 +685,28 @@ struct DraftPlan {
   int chunks, segments, stages;
 };
 
-// Segments and ring depth of a step.  For each ring depth: as many segments
-// (at most one per two chunks, at most kMaxSegments = one cluster) as keep
-// every CTA of the step resident at once, fewer while the device cannot
-// hold all the step's clusters at once.  A CTA then needs ceil(chunks of its
-// segment / stages) rounds of requests; the plan takes the depth with the
-// fewest rounds (the shallowest of equals, which keeps most CTAs resident).
-template <int HD, bool SLOTS>
+// Segments and ring depth of a step with W-warp CTAs.  For each ring depth:
+// as many segments (at most one per two chunks, at most kMaxSegments = one
+// cluster) as keep every CTA of the step resident at once, fewer while the
+// device cannot hold all the step's clusters at once.  A CTA then needs
+// ceil(chunks of its segment / stages) rounds of requests; the plan takes
+// the depth with the fewest rounds (the shallowest of equals, which keeps
+// most CTAs resident).
+template <int HD, bool SLOTS, int W>
 bool make_draft_plan(int batch, int num_kv_heads, int cap, int max_tail, DraftPlan* pl) {
-  pl->chunks = ceil_div(cap + max_tail, kChunk);
+  using Lay = DraftLayout<HD, W>;
+  pl->chunks = ceil_div(cap + max_tail, Lay::kChunk);
   const long long units = (long long)batch * num_kv_heads;
   long long best_rounds = -1;
-  for (int st = kMinStages; st <= kMaxStages; ++st) {
-    const int occ = draft_occupancy<HD, SLOTS>(st);
+  for (int st = kMinStages; st <= Lay::kStagesFit; ++st) {
+    const int occ = draft_occupancy<HD, SLOTS, W>(st);
     if (occ <= 0) continue;
     const long long resident = (long long)device_sm_count() * occ;
     long long S = std::max<long long>(1, resident / units);
     S = std::min<long long>(S, kMaxSegments);
     S = std::min<long long>(S, std::max(1, pl->chunks / 2));
-    while (S > 1 && draft_max_clusters<HD, SLOTS>((int)S, st) < units) --S;
-    if (draft_max_clusters<HD, SLOTS>((int)S, st) <= 0) continue;
+    while (S > 1 && draft_max_clusters<HD, SLOTS, W>((int)S, st) < units) --S;
+    if (draft_max_clusters<HD, SLOTS, W>((int)S, st) <= 0) continue;
     const long long share = (2LL * pl->chunks + 2 * S - 2) / (2 * S - 1);  // chunks of a segment
     const long long rounds = (share + st - 1) / st;
     if (best_rounds < 0 || rounds < best_rounds) {
@@ -702,11 +718,8 @@ bool make_draft_plan(int batch, int num_kv_heads, int cap, int max_tail, DraftPl
   return best_rounds > 0;
 }
 
-template <int HD, bool SLOTS>
-cudaError_t launch_draft_impl(DraftParams p, cudaStream_t stream) {
-  DraftPlan pl;
-  if (!make_draft_plan<HD, SLOTS>(p.batch, p.num_kv_heads, p.cap, p.max_tail, &pl))
-    return cudaErrorInvalidConfiguration;
+template <int HD, bool SLOTS, int W>
+cudaError_t launch_draft_w(DraftParams p, const DraftPlan& pl, cudaStream_t stream) {
   p.segments = pl.segments;
   p.chunks = pl.chunks;
   p.stages = pl.stages;
@@ -719,12 +732,26 @@ cudaError_t launch_draft_impl(DraftParams p, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.segments, p.num_kv_heads, p.batch);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = DraftLayout<HD>::bytes(SLOTS, pl.stages);
+  cfg.blockDim = dim3(DraftLayout<HD, W>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = DraftLayout<HD, W>::bytes(SLOTS, pl.stages);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, sparse_draft_kernel<HD, SLOTS>, p);
+  return cudaLaunchKernelEx(&cfg, sparse_draft_kernel<HD, SLOTS, W>, p);
+}
+
+// CTAs of 4 warps when the step has CTAs to spare for every SM (many
+// (sequence, KV head) pairs); otherwise CTAs of 8 warps, whose gathers
+// draw twice the threads per SM on the few SMs the step occupies.
+template <int HD, bool SLOTS>
+cudaError_t launch_draft_impl(const DraftParams& p, cudaStream_t stream) {
+  DraftPlan p4, p8;
+  const bool ok4 = make_draft_plan<HD, SLOTS, 4>(p.batch, p.num_kv_heads, p.cap, p.max_tail, &p4);
+  const bool ok8 = make_draft_plan<HD, SLOTS, 8>(p.batch, p.num_kv_heads, p.cap, p.max_tail, &p8);
+  const long long ctas4 = ok4 ? (long long)p.batch * p.num_kv_heads * p4.segments : 0;
+  if (ok8 && (!ok4 || ctas4 <= device_sm_count())) return launch_draft_w<HD, SLOTS, 8>(p, p8, stream);
+  if (ok4) return launch_draft_w<HD, SLOTS, 4>(p, p4, stream);
+  return cudaErrorInvalidConfiguration;
 }
 
 template <int HD>
