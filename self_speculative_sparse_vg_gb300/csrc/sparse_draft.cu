@@ -686,12 +686,13 @@ struct DraftPlan {
 };
 
 // Segments and ring depth of a step with W-warp CTAs.  For each ring depth:
-// as many segments (at most one per two chunks, at most kMaxSegments = one
-// cluster) as keep every CTA of the step resident at once, fewer while the
-// device cannot hold all the step's clusters at once.  A CTA then needs
-// ceil(chunks of its segment / stages) rounds of requests; the plan takes
-// the depth with the fewest rounds (the shallowest of equals, which keeps
-// most CTAs resident).
+// as many segments as keep every CTA of the step resident at once, at most
+// kMaxSegments (one cluster) and at most (chunks + 1) / 2 (two chunks a
+// segment, one for the leader's half share), fewer while the device cannot
+// hold all the step's clusters at once.  A CTA then needs ceil(chunks of
+// its segment / stages) rounds of requests; the plan takes the depth with
+// the fewest rounds (the shallowest of equals, which keeps most CTAs
+// resident).
 template <int HD, bool SLOTS, int W>
 bool make_draft_plan(int batch, int num_kv_heads, int cap, int max_tail, DraftPlan* pl) {
   using Lay = DraftLayout<HD, W>;
@@ -704,7 +705,7 @@ bool make_draft_plan(int batch, int num_kv_heads, int cap, int max_tail, DraftPl
     const long long resident = (long long)device_sm_count() * occ;
     long long S = std::max<long long>(1, resident / units);
     S = std::min<long long>(S, kMaxSegments);
-    S = std::min<long long>(S, std::max(1, pl->chunks / 2));
+    S = std::min<long long>(S, std::max(1, (pl->chunks + 1) / 2));
     while (S > 1 && draft_max_clusters<HD, SLOTS, W>((int)S, st) < units) --S;
     if (draft_max_clusters<HD, SLOTS, W>((int)S, st) <= 0) continue;
     const long long share = (2LL * pl->chunks + 2 * S - 2) / (2 * S - 1);  // chunks of a segment
