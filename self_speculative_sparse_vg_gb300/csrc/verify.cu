@@ -5,7 +5,9 @@
 // rows over the whole cache, and it writes only two pre-softmax logit rows
 // (first draft token, bonus token) for the prefix positions.
 //
-// Design (one CTA per (KV split, KV head, sequence)):
+// Design (a unit of work is one KV split of one KV head of one sequence; one
+// CTA per unit, or, when the units outnumber the SMs, one persistent CTA per
+// SM walking a unit list built on the device from the lengths):
 //  * The g query heads x R verify rows of one KV head are packed into the M
 //    dimension of 5th-generation tensor-core MMAs (tcgen05.mma, bf16 in, fp32
 //    accumulators in tensor memory, M padded to 128), so every K/V page is
