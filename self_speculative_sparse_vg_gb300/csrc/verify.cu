@@ -120,7 +120,7 @@ constexpr int kSCol = 0, kOCol = 2 * kVTile, kQCol = kOCol + 128;
 constexpr float kRescaleLog2 = 32.f;
 constexpr int kChunk = 32;             // columns a softmax pass holds in registers
 constexpr int kMaxPersistBatch = 64;   // sequences a persistent CTA's unit table holds
-constexpr int kCapStride = kChunk + 1; // floats per staged capture row
+constexpr int kCapStride = kChunk + 4; // floats per staged capture row (16-byte rows, no bank conflicts)
 
 template <int HD>
 struct VerifyLayout {
@@ -301,7 +301,9 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
         if (cap_two) {
           if (lane < nrows) {
 #pragma unroll
-            for (int j = 0; j < kChunk; ++j) cap_w[lane * kCapStride + j] = s[j] * p.scale;
+            for (int j = 0; j < kChunk; j += 4)
+              *reinterpret_cast<float4*>(cap_w + lane * kCapStride + j) =
+                  make_float4(s[j] * p.scale, s[j + 1] * p.scale, s[j + 2] * p.scale, s[j + 3] * p.scale);
           }
           __syncwarp();
           if (kpos + lane < L) {
