@@ -276,6 +276,9 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
     }
 
     // -------- pass 1: capture (prefix positions) and the row maximum
+    // (dense: a tile whose columns every row of the warp attends skips the
+    // per-column masks; padding lanes hold zero scores and are never read)
+    const bool full_tile = !SP && __all_sync(0xffffffffu, m >= M || rem >= COLS - 1);
     float s[kChunk];
     float call[NCH];                   // Collect-All column sums of this lane
     float mx = -INFINITY;
@@ -344,9 +347,20 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
           call[k] = cv[0];
         }
       }
+      if (full_tile) {  // every column attended: a tree, no masks
+        float t[kChunk / 2];
 #pragma unroll
-      for (int j = 0; j < kChunk; ++j)
-        if (SP ? ((vbits[k] >> j) & 1u) != 0 : k * kChunk + j <= rem) mx = fmaxf(mx, s[j]);
+        for (int j = 0; j < kChunk / 2; ++j) t[j] = fmaxf(s[j], s[j + kChunk / 2]);
+#pragma unroll
+        for (int w = kChunk / 4; w > 0; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+        mx = fmaxf(mx, t[0]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j)
+          if (SP ? ((vbits[k] >> j) & 1u) != 0 : k * kChunk + j <= rem) mx = fmaxf(mx, s[j]);
+      }
     }
     if (cap_all && cpos < L) {
       // across the copy's warps, in order, through shared memory
@@ -417,15 +431,31 @@ __device__ __forceinline__ void verify_softmax(const VerifyParams& p, const Veri
 #pragma unroll
     for (int k = 0; k < NCH; ++k) {
       if (NCH > 1) tmem_ld32(sbuf + col0 + k * kChunk, s);
+      if (full_tile) {  // no masks; the row sum as a tree
+        float ps[kChunk / 2];
 #pragma unroll
-      for (int j = 0; j < kChunk / 2; ++j) {
-        const int jj = k * kChunk + 2 * j;
-        const bool v0 = SP ? ((vbits[k] >> (2 * j)) & 1u) != 0 : jj <= rem;
-        const bool v1 = SP ? ((vbits[k] >> (2 * j + 1)) & 1u) != 0 : jj + 1 <= rem;
-        const float p0 = v0 ? ex2(fmaf(s[2 * j], p.scale_log2, nref)) : 0.f;
-        const float p1 = v1 ? ex2(fmaf(s[2 * j + 1], p.scale_log2, nref)) : 0.f;
-        lsum += p0 + p1;
-        pk[k][j] = pack_bf16(p0, p1);
+        for (int j = 0; j < kChunk / 2; ++j) {
+          const float p0 = ex2(fmaf(s[2 * j], p.scale_log2, nref));
+          const float p1 = ex2(fmaf(s[2 * j + 1], p.scale_log2, nref));
+          ps[j] = p0 + p1;
+          pk[k][j] = pack_bf16(p0, p1);
+        }
+#pragma unroll
+        for (int w = kChunk / 4; w > 0; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
+        lsum += ps[0];
+      } else {
+#pragma unroll
+        for (int j = 0; j < kChunk / 2; ++j) {
+          const int jj = k * kChunk + 2 * j;
+          const bool v0 = SP ? ((vbits[k] >> (2 * j)) & 1u) != 0 : jj <= rem;
+          const bool v1 = SP ? ((vbits[k] >> (2 * j + 1)) & 1u) != 0 : jj + 1 <= rem;
+          const float p0 = v0 ? ex2(fmaf(s[2 * j], p.scale_log2, nref)) : 0.f;
+          const float p1 = v1 ? ex2(fmaf(s[2 * j + 1], p.scale_log2, nref)) : 0.f;
+          lsum += p0 + p1;
+          pk[k][j] = pack_bf16(p0, p1);
+        }
       }
     }
     tc_fence_before();  // every read of S precedes the P writes over it
