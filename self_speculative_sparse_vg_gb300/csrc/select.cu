@@ -296,8 +296,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
         const uint32_t key = in ? keys[j] : 0u;
         const bool v = in && ((key & mask) == prefix);
         const int dig = v ? (int)((key >> shift) & 255u) : -1;
-        const unsigned grp = __match_any_sync(0xffffffffu, dig);
-        if (v && lane == __ffs(grp) - 1) atomicAdd(&hb[dig], (uint32_t)__popc(grp));
+        // lane 0's digit is counted with one ballot (keys crowd into few
+        // bins, the first pass's into one or two), the others one by one
+        const int d0 = __shfl_sync(0xffffffffu, dig, 0);
+        const unsigned same = __ballot_sync(0xffffffffu, dig == d0);
+        if (lane == 0 && d0 >= 0) atomicAdd(&hb[d0], (uint32_t)__popc(same));
+        if (v && dig != d0) atomicAdd(&hb[dig], 1u);
       }
       __syncthreads();
       if (!peers_ready) {
