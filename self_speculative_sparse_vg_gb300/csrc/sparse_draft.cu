@@ -9,11 +9,12 @@
 //
 // Design: one kernel per draft step.  The attended list of a (sequence, KV
 // head) -- the selection, then the tail [tail_start, cur_len) -- is cut into
-// 64-entry chunks, and the chunks into S segments; one CTA per (segment, KV
-// head, sequence), and the S CTAs of a (sequence, KV head) form one
-// thread-block cluster (S <= 16).  S is planned on the host so that the
-// step's CTAs are resident at once; segment 0 (the cluster's leader) takes
-// half a share of the chunks, the others a full share each.
+// chunks of 16 W entries (W = 4 or 8 warps per CTA), and the chunks into S
+// segments; one CTA per (segment, KV head, sequence), and the S CTAs of a
+// (sequence, KV head) form one thread-block cluster (S <= 16).  W, S and the
+// ring depth are planned on the host per launch so that the step's CTAs are
+// resident at once; segment 0 (the cluster's leader) takes half a share of
+// the chunks, the others a full share each.
 //  * Addresses cost one round trip.  With the cache slots the selector wrote
 //    beside the positions (physical page * 16 + offset, translated once per
 //    selection) a chunk loads its slots and positions (the positions are
@@ -103,7 +104,7 @@ struct DraftLayout {
                 "the O stash reuses the ring");
   static_assert((size_t)(kMaxSegments - 1) * kRecBytes <= (size_t)kMinRing,
                 "the leader receives the other segments' records in its ring");
-  static_assert(kRowBytes % 16 == 0 && kTileBytes % 16 == 0, "16-byte bulk-copy destinations");
+  static_assert(kRowBytes % 16 == 0 && kTileBytes % 16 == 0, "16-byte copy destinations");
 };
 
 // Sequence-level checks; false if the sequence is skipped.
