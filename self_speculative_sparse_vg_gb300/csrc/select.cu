@@ -38,7 +38,8 @@ namespace cg = cooperative_groups;
 namespace vg {
 namespace {
 
-constexpr int kSelThreads = 1024;
+// CTAs of the selection cluster have NT = 1024 threads, or 512 (two CTAs per
+// SM) when a batch's clusters would not all be resident otherwise.
 constexpr int kMaxCluster = 16;
 constexpr int kTargetSlice = 2048;
 constexpr int kMaxSlice = 16384;  // keys per CTA (64 KB of shared memory)
@@ -174,7 +175,8 @@ __global__ void __launch_bounds__(kScoreThreads) select_score_kernel(const Selec
   p.keys_ws[((size_t)b * p.rows + row) * p.max_prefix + j] = score_key(row_score(p, b, row, j));
 }
 
-__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectParams p) {
+template <int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(const SelectParams p) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -251,18 +253,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
     // every capture load of the four issued before the first add
     const size_t Lm = p.max_prefix;
     const float* G = p.capture + (size_t)b * p.num_kv_heads * Lm + (p.per_head ? (size_t)row * Lm : 0);
-    for (int j0 = tid; j0 < n_loc; j0 += 4 * kSelThreads) {
+    for (int j0 = tid; j0 < n_loc; j0 += 4 * NT) {
       float v[4][8];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * kSelThreads;
+        const int j = j0 + u * NT;
 #pragma unroll
         for (int t = 0; t < 8; ++t)
           v[u][t] = (t < terms && j < n_loc) ? __ldg(G + (size_t)t * Lm + lo + j) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * kSelThreads;
+        const int j = j0 + u * NT;
         float acc = v[u][0];
 #pragma unroll
         for (int t = 1; t < 8; ++t)
@@ -311,8 +313,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
       // push this CTA's histogram (64 pieces of 16 bytes) into slot `rank` of
       // every CTA's region for this pass
       uint32_t* rp = recv + pass * kMaxCluster * 256;
-      if (tid < 64 * C) {
-        const int dst = tid >> 6, piece = tid & 63;
+      for (int i = tid; i < 64 * C; i += NT) {
+        const int dst = i >> 6, piece = i & 63;
         const uint4 hv = reinterpret_cast<const uint4*>(hb)[piece];
         st_async_v4(mapa_shared(smem_u32(rp + rank * 256 + piece * 4), dst), hv,
                     mapa_shared(smem_u32(&mb[pass]), dst));
@@ -372,7 +374,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
   // Warp w owns the contiguous key range [w * 32 * per, (w + 1) * 32 * per)
   // of this CTA's slice, read 32 at a time; counts go through ballots, and
   // the warps are ordered by one exclusive scan per quantity.
-  const int per = (n_loc + kSelThreads - 1) / kSelThreads;  // keys per lane
+  const int per = (n_loc + NT - 1) / NT;  // keys per lane
+  constexpr int kWarps = NT / 32;
   const int wid = tid >> 5;
   const int wbase = wid * 32 * per;
   const unsigned lt_mask = (1u << lane) - 1u;
@@ -392,8 +395,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
     wb[32 + wid] = gt_w;
   }
   __syncthreads();
-  if (wid == 0) {  // 32 warps: exclusive scan of the per-warp == T counts, totals
-    const int e = wb[lane], gtv = wb[32 + lane];
+  if (wid == 0) {  // exclusive scan of the per-warp == T counts, totals
+    const int e = lane < kWarps ? wb[lane] : 0, gtv = lane < kWarps ? wb[32 + lane] : 0;
     int incl = e, gsum = gtv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectPara
     if (lane == 0) wb[96 + wid] = sel_w;
     __syncthreads();
     if (wid == 0) {
-      const int v = wb[96 + lane];
+      const int v = lane < kWarps ? wb[96 + lane] : 0;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -506,27 +509,32 @@ size_t select_smem_bytes(int slice) {
          align_up(((size_t)slice / 16 + 2) * 4, 16);
 }
 
+template <int NT>
+bool set_select_attributes_nt() {
+  return cudaFuncSetAttribute(select_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)select_smem_bytes(kMaxSlice)) == cudaSuccess &&
+         cudaFuncSetAttribute(select_kernel<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                              1) == cudaSuccess;
+}
+
 bool set_select_attributes() {
   static bool done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && done[dev]) return true;
-  if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)select_smem_bytes(kMaxSlice)) != cudaSuccess ||
-      cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-          cudaSuccess)
-    return false;
+  if (!set_select_attributes_nt<1024>() || !set_select_attributes_nt<512>()) return false;
   if (dev < 64) done[dev] = true;
   return true;
 }
 
-// Clusters of C CTAs (slice of `slice` keys each) the device holds at once.
-int select_max_clusters(int C, int slice) {
+// Clusters of C CTAs of NT threads (slice of `slice` keys each) the device
+// holds at once.
+int select_max_clusters(int C, int slice, int NT) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int>, int> memo;
+  static std::map<std::tuple<int, int, int, int>, int> memo;
   int dev = 0;
   cudaGetDevice(&dev);
-  const auto key = std::make_tuple(dev, C, slice);
+  const auto key = std::make_tuple(dev, C, slice, NT);
   {
     std::lock_guard<std::mutex> g(mu);
     const auto it = memo.find(key);
@@ -534,7 +542,7 @@ int select_max_clusters(int C, int slice) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, 1, 1);
-  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = select_smem_bytes(slice);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -544,7 +552,10 @@ int select_max_clusters(int C, int slice) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, select_kernel, &cfg) != cudaSuccess) {
+  const cudaError_t e =
+      NT == 512 ? cudaOccupancyMaxActiveClusters(&n, select_kernel<512>, &cfg)
+                : cudaOccupancyMaxActiveClusters(&n, select_kernel<1024>, &cfg);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -553,23 +564,32 @@ int select_max_clusters(int C, int slice) {
   return n;
 }
 
-// Cluster size and keys per CTA for `clusters` selection rows of max_prefix
-// positions: slices of about kTargetSlice keys in clusters of up to
-// kMaxCluster CTAs, halved while the rows' clusters would not all be resident
-// at once (a second wave costs a whole selection) and the slice still fits.
-bool select_shape(int max_prefix, long long clusters, int* C, int* slice) {
+// Cluster size, keys per CTA and threads per CTA for `clusters` selection
+// rows of max_prefix positions: slices of about kTargetSlice keys in
+// clusters of up to kMaxCluster CTAs of 1024 threads.  While the rows'
+// clusters would not all be resident at once (a second wave costs a whole
+// selection): CTAs of 512 threads (two per SM), else clusters halved, as
+// long as the slice still fits.
+bool select_shape(int max_prefix, long long clusters, int* C, int* slice, int* nt) {
   int c = 1;
   while (c < kMaxCluster && ceil_div(max_prefix, c) > kTargetSlice) c *= 2;
   int s = align_up(ceil_div(max_prefix, c), 4);
   if (s > kMaxSlice) return false;
-  while (c > 1) {
+  int t = 1024;
+  while (c > 1 && clusters > 1) {
+    if (clusters <= select_max_clusters(c, s, 1024)) break;
+    if (clusters <= select_max_clusters(c, s, 512)) {
+      t = 512;
+      break;
+    }
     const int s2 = align_up(ceil_div(max_prefix, c / 2), 4);
-    if (s2 > kMaxSlice || clusters <= 1 || clusters <= select_max_clusters(c, s)) break;
+    if (s2 > kMaxSlice) break;
     c /= 2;
     s = s2;
   }
   *C = c;
   *slice = s;
+  *nt = t;
   return true;
 }
 
@@ -607,9 +627,9 @@ extern "C" int vg_select_launches(int capture_mode, int batch, int num_kv_heads,
   if (capture_mode != VG_CAPTURE_GROUP_SUM && capture_mode != VG_CAPTURE_ROWS &&
       capture_mode != VG_CAPTURE_ALL_ROWS)
     return 0;
-  int C, slice;
-  if (!select_shape(max_prefix, 1, &C, &slice) || !set_select_attributes()) return 0;
-  select_shape(max_prefix, (long long)batch * (per_head ? num_kv_heads : 1), &C, &slice);
+  int C, slice, nt;
+  if (!select_shape(max_prefix, 1, &C, &slice, &nt) || !set_select_attributes()) return 0;
+  select_shape(max_prefix, (long long)batch * (per_head ? num_kv_heads : 1), &C, &slice, &nt);
   return select_fused(capture_mode, per_head, num_kv_heads, slice) ? 1 : 2;
 }
 
@@ -661,12 +681,12 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
   if (num_q_heads / num_kv_heads > 8) return VG_ERR_UNSUPPORTED;
   const long long budget = (long long)n_sink + n_recent + top_k;
   if (cap < std::min<long long>(max_prefix, budget)) return VG_ERR_INVALID_ARGUMENT;
-  int C, slice;
-  if (!select_shape(max_prefix, 1, &C, &slice)) return VG_ERR_UNSUPPORTED;
+  int C, slice, nt;
+  if (!select_shape(max_prefix, 1, &C, &slice, &nt)) return VG_ERR_UNSUPPORTED;
   const size_t ws_need = vg_select_workspace_bytes(batch, num_kv_heads, max_prefix, per_head);
   if (!workspace || workspace_bytes < ws_need) return VG_ERR_WORKSPACE_TOO_SMALL;
   if (!set_select_attributes()) return VG_ERR_LAUNCH;
-  select_shape(max_prefix, (long long)batch * (per_head ? num_kv_heads : 1), &C, &slice);
+  select_shape(max_prefix, (long long)batch * (per_head ? num_kv_heads : 1), &C, &slice, &nt);
 
   SelectParams p;
   p.capture = capture;
@@ -710,7 +730,7 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
     return VG_ERR_LAUNCH;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, p.rows, batch);
-  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.blockDim = dim3(nt, 1, 1);
   cfg.dynamicSmemBytes = select_smem_bytes(slice);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -722,6 +742,7 @@ static vg_status select_impl(const float* capture, int capture_mode, int n_rows,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel, p);
+  const cudaError_t e = nt == 512 ? cudaLaunchKernelEx(&cfg, select_kernel<512>, p)
+                                  : cudaLaunchKernelEx(&cfg, select_kernel<1024>, p);
   return e == cudaSuccess ? VG_OK : VG_ERR_LAUNCH;
 }
