@@ -554,8 +554,8 @@ __global__ void __launch_bounds__(32 * W) sparse_draft_kernel(const DraftParams 
     cluster_arrive_release();  // the records have landed: the senders may leave
     if (got) {
       const float* recs = reinterpret_cast<const float*>(ring);
-      // weights: warp w takes query heads w, w + 4; lane q < n_send holds
-      // pushed record q, lane 16 the leader's own (m = -inf without work)
+      // weights: warp w takes query heads w, w + W, ...; lane q < n_send
+      // holds pushed record q, lane 16 the leader's own (m = -inf without work)
       for (int qi = warp; qi < g; qi += kWarps) {
         float mq = -INFINITY, lq = 0.f;
         if (lane < n_send) {
