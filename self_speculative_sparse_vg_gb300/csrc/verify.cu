@@ -1055,16 +1055,21 @@ template <int HD>
 __global__ void __launch_bounds__(kMergeThreads) verify_merge_kernel(const VerifyParams p) {
   __shared__ __align__(16) float smem_f[kMergeSmemFloats];
   const int m = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // The length and the union size are read before waiting for the verify
+  // grid: this kernel's predecessor is always that grid, which writes
+  // neither (it waits for its own predecessors before it lets this kernel
+  // launch), so the read overlaps the verify tail instead of following it.
+  const int L = p.prefix_lens[b];
+  const int u_cnt = p.u_count ? p.u_count[b] : 0;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const int L = p.prefix_lens[b];
   if (L < 1 || L > p.max_prefix ||
       (L + p.n_rows + kPageSize - 1) / kPageSize > p.max_pages_per_seq)
     return;  // the verify kernel skipped this sequence (and flagged it)
   const int M = p.m_rows, S = p.splits;
   // splits with work: dense, split s streams tiles [s tps, (s + 1) tps) of
   // the sequence's; sparse, split s takes union tiles s, s + S, ...
-  const int tiles_b = p.u_count ? (min(p.u_count[b], p.u_max) + kVTile / kPageSize - 1) / (kVTile / kPageSize)
+  const int tiles_b = p.u_count ? (min(u_cnt, p.u_max) + kVTile / kPageSize - 1) / (kVTile / kPageSize)
                                 : (L + p.n_rows + kVTile - 1) / kVTile;
   const int s_work = p.u_count ? min(S, tiles_b)
                                : min(S, (tiles_b + p.tiles_per_split - 1) / p.tiles_per_split);
