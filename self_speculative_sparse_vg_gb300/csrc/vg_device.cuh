@@ -478,7 +478,7 @@ __device__ __forceinline__ float safe_ref(float m) { return m == -INFINITY ? 0.f
 // normaliser from the (m, l) pairs with shuffles and publishes them behind
 // one barrier; the G split groups are then reduced in shared memory behind
 // one more.
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;
 constexpr int kMergePer = 8;
 
 constexpr int kMergeSmemFloats = 8 + 128 + 4 * kMergeThreads;
