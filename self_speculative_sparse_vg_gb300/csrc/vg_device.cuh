@@ -221,20 +221,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Four rows of a 2-D tiled tensor map (box = columns x 1 row) gathered into
-// shared memory: the rows land one after another, each box-width bytes, with
-// the map's swizzle.  Row coordinates past the map's extent read zeros;
-// completion counted on `bar`.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                            int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
 // 1-D bulk copy global -> shared (size and both addresses multiples of 16 B),
 // completion counted on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

@@ -90,45 +90,6 @@ bool page_pool_tensor_map(const void* base, int num_pages, int num_kv_heads, int
   return true;
 }
 
-bool page_pool_row_map(const void* base, int num_pages, int num_kv_heads, int head_dim,
-                       CUtensorMap* out) {
-  constexpr int kEntries = 16;
-  static MapEntry cache[kEntries];
-  static int next = 0;
-  static std::mutex mu;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    for (auto& e : cache)
-      if (e.base == base && e.num_pages == num_pages && e.num_kv_heads == num_kv_heads &&
-          e.head_dim == head_dim && e.device == dev) {
-        *out = e.map;
-        return true;
-      }
-  }
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const long long rows = (long long)num_pages * num_kv_heads * kPageSize;
-  if (rows >= (1ll << 31)) return false;  // row coordinates are 32-bit
-  CUtensorMap map;
-  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-  cuuint32_t box[2] = {(cuuint32_t)head_dim, 1};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return false;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    cache[next] = MapEntry{base, num_pages, num_kv_heads, head_dim, dev, map};
-    next = (next + 1) % kEntries;
-  }
-  *out = map;
-  return true;
-}
-
 vg_status check_paged_kv(const vg_paged_kv* kv) {
   if (!kv || !kv->k_pages || !kv->v_pages || !kv->page_table) return VG_ERR_INVALID_ARGUMENT;
   if (kv->num_pages <= 0 || kv->max_pages_per_seq <= 0 || kv->num_kv_heads <= 0)

@@ -28,13 +28,6 @@ uint64_t wait_report_ns();
 bool page_pool_tensor_map(const void* base, int num_pages, int num_kv_heads, int head_dim,
                           CUtensorMap* out);
 
-// 2-D TMA descriptor over a page pool viewed as rows: [num_pages *
-// num_kv_heads * 16][head_dim] bf16, box = head_dim x 1, no swizzle, for
-// tile::gather4 loads of four arbitrary rows.  Cached per (pointer, shape).
-// Returns false on failure.
-bool page_pool_row_map(const void* base, int num_pages, int num_kv_heads, int head_dim,
-                       CUtensorMap* out);
-
 // Basic checks of a vg_paged_kv; VG_OK or an error status.
 vg_status check_paged_kv(const vg_paged_kv* kv);
 
