@@ -43,6 +43,7 @@ namespace {
 constexpr int kMaxCluster = 16;
 constexpr int kTargetSlice = 2048;
 constexpr int kMaxSlice = 16384;  // keys per CTA (64 KB of shared memory)
+static_assert(kMaxSlice / 512 <= 32, "a lane's keys fit one 32-bit mask");
 constexpr int kFusedLoads = 32768;  // capture loads per CTA up to which the cluster scores
 
 struct SelectParams {
@@ -445,6 +446,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(const SelectParam
     const int gt_before = ctl[2], eq_before = ctl[3];
     const int eq_rank0 = eq_before + wb[64 + wid];  // rank of this warp's first == T key
     int sel_w = 0, eq_run = eq_rank0;
+    uint32_t selbits = 0;  // bit i: this lane's key of round i is kept (per <= 32)
     for (int i = 0; i < per; ++i) {
       const int j = wbase + i * 32 + lane;
       const int pos = lo + j;
@@ -453,6 +455,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(const SelectParam
       const bool is_eq = in && k == T;
       const unsigned eb = __ballot_sync(0xffffffffu, is_eq);
       const bool sel = (in && k > T) || (is_eq && eq_run + __popc(eb & lt_mask) < krem);
+      selbits |= (uint32_t)sel << i;
       sel_w += __popc(__ballot_sync(0xffffffffu, sel));
       eq_run += __popc(eb);
     }
@@ -471,19 +474,13 @@ __global__ void __launch_bounds__(NT, 1024 / NT) select_kernel(const SelectParam
     __syncthreads();
     const int slot0 = p.n_sink + gt_before + min(eq_before, krem) + wb[128 + wid];
     int sel_run = 0;
-    eq_run = eq_rank0;
     for (int i = 0; i < per; ++i) {
-      const int j = wbase + i * 32 + lane;
-      const int pos = lo + j;
-      const bool in = j < n_loc && pos >= c_lo && pos < c_hi;
-      const uint32_t k = in ? (keys[j] & mask) : 0u;
-      const bool is_eq = in && k == T;
-      const unsigned eb = __ballot_sync(0xffffffffu, is_eq);
-      const bool sel = (in && k > T) || (is_eq && eq_run + __popc(eb & lt_mask) < krem);
+      const bool sel = (selbits >> i) & 1u;
       const unsigned sbal = __ballot_sync(0xffffffffu, sel);
-      if (sel) put_kept(p, out, sout, pt_s, pt0, slot0 + sel_run + __popc(sbal & lt_mask), pos);
+      if (sel)
+        put_kept(p, out, sout, pt_s, pt0, slot0 + sel_run + __popc(sbal & lt_mask),
+                 lo + wbase + i * 32 + lane);
       sel_run += __popc(sbal);
-      eq_run += __popc(eb);
     }
   }
   // sink and recent positions, by the CTA whose slice holds them
