@@ -40,10 +40,15 @@ SMALL = dict(
     short=dict(prefix_lens=(1, 15, 16, 63, 64, 65, 130), batch=7, top_k=8, n_sink=2, n_recent=4),
     budget_all=dict(prefix_lens=(40, 83), top_k=64, n_sink=4, n_recent=16),
     ties=dict(prefix_lens=(700,), batch=1, top_k=33),
-    # batch * KV heads > 16: 64-entry chunks, one CTA each, and the merge kernel
+    # 24 (sequence, KV head) pairs: the sparse draft's 4-warp CTAs
     many_pairs=dict(batch=3, prefix_lens=(1000, 517, 333), num_q_heads=32, num_kv_heads=8),
-    # a list longer than one 16-CTA cluster covers: cluster partials + merge kernel
+    # one long list: a 16-CTA draft cluster merging 15 records into its leader
     long_list=dict(batch=1, prefix_lens=(6000,), num_q_heads=4, num_kv_heads=1, top_k=5500),
+)
+# drafts without cache slots on a page table longer than the draft kernel
+# stages in shared memory (2048 entries): pages looked up entry by entry
+NO_SLOTS_EXTRA = dict(
+    long_table=dict(batch=1, prefix_lens=(40000,), num_q_heads=4, num_kv_heads=1, top_k=300),
 )
 
 
@@ -65,16 +70,17 @@ def test_small_step(name, mode, per_head):
 
 
 @pytest.mark.parametrize("name", ["base", "d64", "g8", "k0", "pages_shuffled", "short",
-                                  "many_pairs", "long_list"])
+                                  "many_pairs", "long_list", "long_table"])
 @pytest.mark.parametrize("per_head", [False, True])
 def test_draft_without_slots(name, per_head):
     """Drafts on positions alone (no cache slots: the kernel stages the page
-    table itself) against the oracle, on the GPU's selection and on
-    generator-made index lists."""
+    table itself, or looks pages up one by one when the table is long)
+    against the oracle, on the GPU's selection and on generator-made index
+    lists."""
     _require_gpu()
     from self_speculative_sparse_vg_gb300.step import DecodeStep
     from self_speculative_sparse_vg_gb300.workloads import make_inputs, small_spec
-    spec = small_spec(**SMALL[name])
+    spec = small_spec(**{**SMALL, **NO_SLOTS_EXTRA}[name])
     inp = make_inputs(spec)
     st = DecodeStep.create(inp, "cuda", per_head=per_head, use_slots=False)
     st.run()
