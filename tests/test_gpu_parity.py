@@ -44,6 +44,9 @@ SMALL = dict(
     many_pairs=dict(batch=3, prefix_lens=(1000, 517, 333), num_q_heads=32, num_kv_heads=8),
     # one long list: a 16-CTA draft cluster merging 15 records into its leader
     long_list=dict(batch=1, prefix_lens=(6000,), num_q_heads=4, num_kv_heads=1, top_k=5500),
+    # head_dim 64 with many pairs: the 4-warp draft CTAs at d = 64
+    many_pairs_d64=dict(batch=6, prefix_lens=(2000, 1517, 1333, 900, 2100, 1700), head_dim=64,
+                        num_q_heads=32, num_kv_heads=8, top_k=512),
 )
 # drafts without cache slots on a page table longer than the draft kernel
 # stages in shared memory (2048 entries): pages looked up entry by entry
